@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA sparse-MLA hot path on GB300.
+
+One step = one pass of the whole path over one batch: causal top-k over the
+indexer scores, the sparse MLA Partial over the selected FP8 rows and, when
+the launch splits the KV range, the Combine.  Inputs are seeded synthetic
+tensors with the shapes of the GLM-5.3-Flash serving workloads (default: 128
+decode requests at 64K context sharing a 99.9% prefix, top-k 2048, 64 heads,
+latent 512 + rope 64, FP8 E4M3 KV with per-token scales).
+
+Prints one JSON line: whole-job query-tokens/s with inputs resident in HBM
+(`value`), the same through host buffers with the copies timed (`e2e`), the
+dominant kernel against its roofline, the fp64 oracle's speed on the host
+cores (`cpu_baseline`) and the SM clocks seen during the timed region.
+`--impl reference` times the fp64 oracle itself, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA query-tokens/s (top-k 2048, FP8 KV) and % of GB300 roofline"
+UNIT = "query-tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+NOMINAL_TFLOPS, NOMINAL_GBS = 2250.0, 8000.0
+FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
+
+# DRAM bytes (read + write) per launch of the attention kernel, from one ncu
+# capture, keyed by the SHA-1 of the kernel source it was taken on.  A stale
+# entry (the kernel changed since) is reported as null.
+TRAFFIC_BY_SOURCE: dict[str, dict] = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_64k_prefix99.9")
+    ap.add_argument("--splits", type=int, default=0, help="KV splits (0 = library's rule)")
+    ap.add_argument("--cpu-sample", type=int, default=64, help="query tokens the oracle baseline times")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def algorithmic(w, q_pos_host):
+    """FLOPs and bytes of one pass, counted from the method's definition:
+    per query token with k_eff = min(k, visible) selected rows,
+    FLOPs = 2 H k_eff (dqk + d_latent); bytes of the attention step = gathered
+    rows + scales + Q + O (bf16) + LSE + indices read; the top-k step reads the
+    visible scores and writes k indices."""
+    H, dqk, dl, k = w.heads, w.dqk, w.d_latent, w.k
+    flops = bytes_fwd = bytes_topk = 0
+    for p in q_pos_host:
+        vis = int(p) + 1
+        ke = min(k, vis)
+        flops += 2 * H * ke * (dqk + dl)
+        bytes_fwd += ke * (dqk + 4) + H * dqk * 2 + H * dl * 2 + H * 4 + ke * 4
+        bytes_topk += vis * 4 + k * 4
+    return flops, bytes_fwd, bytes_topk
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return {"hbm_gbs": FALLBACK_GBS, "bf16_tflops": FALLBACK_TFLOPS, "bf16_tflops_sustained": None,
+                "source": "fallback"}
+
+    def find(pred):
+        stack = [d]
+        while stack:
+            x = stack.pop()
+            if isinstance(x, dict):
+                for kk, v in x.items():
+                    if isinstance(v, (int, float)) and pred(kk.lower()):
+                        return float(v)
+                    if isinstance(v, (dict, list)):
+                        stack.append(v)
+            elif isinstance(x, list):
+                stack.extend(x)
+        return None
+
+    hbm = find(lambda s: "hbm" in s and ("gbs" in s or "gb_s" in s or "gbps" in s))
+    bf = find(lambda s: "bf16" in s and "tflops" in s and "sustained" not in s)
+    bfs = find(lambda s: "bf16" in s and "sustained" in s)
+    return {"hbm_gbs": hbm or FALLBACK_GBS, "bf16_tflops": bf or FALLBACK_TFLOPS, "bf16_tflops_sustained": bfs,
+            "source": "measured" if hbm else "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None, out_path: str | None):
+        self.uuid = uuid
+        self.path = out_path
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w") if self.path else subprocess.PIPE
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        if self.path:
+            self.f.close()
+            self.text = open(self.path).read()
+        else:
+            self.text = out or ""
+        return False
+
+    def summary(self):
+        rows = []
+        for line in self.text.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            rows.append(parts)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u.replace("GPU-", "")
+    except Exception:
+        return None
+
+
+def run_oracle_sample(w, host, rows, nthreads=0):
+    """Oracle top-k + attention over the given query tokens; returns seconds."""
+    import numpy as np
+    import oracle
+
+    rows = np.asarray(rows)
+    t0 = time.perf_counter()
+    idx = oracle.topk(host["scores"][rows], host["q_pos"][rows], w.k, nthreads=nthreads)
+    oracle.sparse_mla(host["q"][rows], host["kv"], host["kv_scale"], host["block_table"], host["q_req"][rows], idx,
+                      d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale,
+                      nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def host_copies(inp):
+    import torch
+    return {"scores": inp.scores.cpu().numpy(), "q_pos": inp.q_pos.cpu().numpy(),
+            "q": inp.q.view(torch.int16).cpu().numpy(), "kv": inp.kv.cpu().numpy(),
+            "kv_scale": inp.kv_scale.cpu().numpy(), "block_table": inp.block_table.cpu().numpy(),
+            "q_req": inp.q_req.cpu().numpy()}
+
+
+def workload_config(w, splits, extra=None):
+    cfg = {"workload": w.name, "requests": w.num_req, "query_tokens": w.num_q, "heads": w.heads,
+           "d_latent": w.d_latent, "d_rope": w.d_rope, "context": w.ctx, "shared_prefix": w.shared_prefix,
+           "page_size": w.page_size, "top_k": w.k, "kv_splits": splits, "kv_dtype": "fp8_e4m3+fp32 scale/token",
+           "l2": "flushed (512 MiB write) before every timed step"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def bench_reference(args):
+    """The fp64 oracle timed on the host cores (rank 0 only)."""
+    import numpy as np
+    from dsa_sparse_mla_topk_gb300 import workloads as wl
+
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w, device="cpu")
+    import torch
+    host = host_copies(inp)
+    n = min(w.num_q, max(1, args.cpu_sample // 4))
+    rng = np.random.default_rng(0)
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        run_oracle_sample(w, host, rng.choice(w.num_q, size=n, replace=False))
+    total = 0.0
+    for _ in range(args.steps):
+        total += run_oracle_sample(w, host, np.sort(rng.choice(w.num_q, size=n, replace=False)))
+    value = args.steps * n / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, 1, {"sample_query_tokens_per_step": n}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{n} random query tokens of the workload per step (top-k + attention)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_ours(args):
+    import numpy as np
+    import torch
+
+    import dsa_sparse_mla_topk_gb300 as dsa
+    from dsa_sparse_mla_topk_gb300 import build as lib_build
+    from dsa_sparse_mla_topk_gb300 import workloads as wl
+
+    world, rank, local = dist_setup(args)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    lib_build.build()
+    dsa.load_library()
+
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w, device=dev)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    S = args.splits or dsa.pick_num_splits(w.num_q, w.heads, w.d_latent, w.d_rope, w.k, num_sms)
+    q_pos_host = inp.q_pos.cpu().numpy()
+    flops, bytes_fwd, bytes_topk = algorithmic(w, q_pos_host)
+    bytes_path = bytes_fwd + bytes_topk
+
+    stream = torch.cuda.current_stream(dev)
+    bufs = {"idx": torch.empty((w.num_q, w.k), dtype=torch.int32, device=dev),
+            "out": torch.empty((w.num_q, w.heads, w.d_latent), dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty((w.num_q, w.heads), dtype=torch.float32, device=dev)}
+    if S > 1:
+        bufs["o_part"] = torch.empty((S, w.num_q, w.heads, w.d_latent), dtype=torch.float32, device=dev)
+        bufs["lse_part"] = torch.empty((S, w.num_q, w.heads), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        idx = dsa.topk_select(inp.scores, inp.q_pos, w.k, idx=bufs["idx"], dev_status=status, stream=stream)
+        if evs:
+            evs[1].record(stream)
+        if S == 1:
+            dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, num_splits=1,
+                               out=bufs["out"], lse=bufs["lse"], dev_status=status, stream=stream, **kw)
+        else:
+            dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, num_splits=S,
+                               o_part=bufs["o_part"], lse_part=bufs["lse_part"], dev_status=status, stream=stream,
+                               **kw)
+        if evs:
+            evs[2].record(stream)
+        if S > 1:
+            dsa.combine(bufs["o_part"], bufs["lse_part"], out=bufs["out"], lse=bufs["lse"], stream=stream)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clock_path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if os.path.isdir(
+        os.path.join(ROOT, "gpurun_out")) else None
+    sampler = ClockSampler(gpu_uuid(torch, dev), clock_path) if not args.no_clocks else None
+    if sampler:
+        sampler.__enter__()
+    barrier()
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        step(evs[s])
+    barrier()
+    wall = time.perf_counter() - wall0
+    if sampler:
+        sampler.__exit__(None, None, None)
+    t_topk = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
+    t_fwd = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
+    t_comb = [evs[s][2].elapsed_time(evs[s][3]) for s in range(args.steps)]
+    t_step = [evs[s][0].elapsed_time(evs[s][3]) for s in range(args.steps)]
+    total_ms = sum(t_step)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * w.num_q * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through host buffers: copies timed every step ----
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "scores", "q_pos", "q_req", "block_table")}
+        dst = {n: torch.empty_like(getattr(inp, n)) for n in pin}
+        out_h = torch.empty(bufs["out"].shape, dtype=bufs["out"].dtype).pin_memory()
+        lse_h = torch.empty(bufs["lse"].shape, dtype=bufs["lse"].dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+        def e2e_step():
+            for n in pin:
+                dst[n].copy_(pin[n], non_blocking=True)
+            out, lse, _ = dsa.sparse_mla_topk(dst["q"], inp.kv, inp.kv_scale, dst["block_table"], dst["q_req"],
+                                              dst["q_pos"], dst["scores"], w.k, num_splits=S, buffers=bufs,
+                                              dev_status=status, stream=stream, **kw)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        e_ms = 0.0
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            b.synchronize()
+            e_ms += a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * w.num_q * args.steps / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
+               "note": "KV cache resident in HBM; per-step inputs (q, scores, q_pos, q_req, block table) copied "
+                       "from pinned host memory and out + lse read back, inside the timed region"}
+    torch.cuda.synchronize(dev)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peaks = read_peaks()
+    fwd_ms = statistics.mean(t_fwd)
+    src = os.path.join(ROOT, "dsa_sparse_mla_topk_gb300", "csrc", "mla_simt.cu")
+    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    tr = TRAFFIC_BY_SOURCE.get(sha)
+    traffic = None
+    if tr and tr.get("workload") == w.name:
+        traffic = tr["bytes_per_launch"]
+    achieved_gbs = bytes_fwd / (fwd_ms / 1e3) / 1e9
+    ai_path = flops / bytes_path
+    ns_roof = min(NOMINAL_TFLOPS * 1e12, NOMINAL_GBS * 1e9 * ai_path)
+    achieved_flops = flops / (ms_per_step / 1e3)
+    meas_roof = min(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9 * ai_path)
+    launches_per_step = 2 + (1 if S > 1 else 0)
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        host = host_copies(inp)
+        n = min(w.num_q, args.cpu_sample)
+        rows = np.sort(np.random.default_rng(0).choice(w.num_q, size=n, replace=False))
+        secs = run_oracle_sample(w, host, rows)
+        cpu = {"value": n / secs, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
+               "sample": f"{n} of {w.num_q} query tokens (seeded), top-k + attention, fp64 C on all host cores",
+               "seconds": secs}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp32", "data": "synthetic (seeded; shapes of the GLM-5.3-Flash workloads)",
+            "config": workload_config(w, S, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+            "roofline": {"kernel": "sparse_mla_fwd", "bound": "hbm", "achieved": achieved_gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                         "traffic": traffic, "peak_source": peaks["source"],
+                         "algorithmic_bytes_per_launch": bytes_fwd, "avg_launch_ms": fwd_ms,
+                         "achieved_tflops": flops / (fwd_ms / 1e3) / 1e12},
+            "path_roofline": {"ai_flops_per_byte": ai_path, "achieved_tflops": achieved_flops / 1e12,
+                              "frac_nominal": achieved_flops / ns_roof, "frac_measured": achieved_flops / meas_roof,
+                              "nominal_roofline_tflops": ns_roof / 1e12},
+            "kernel_ms": {"topk": statistics.mean(t_topk), "sparse_mla_fwd": fwd_ms,
+                          "combine": statistics.mean(t_comb)},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "clocks": sampler.summary() if sampler else None, "wall_s": wall}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

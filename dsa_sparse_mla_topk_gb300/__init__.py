@@ -1,0 +1,203 @@
+"""GB300 (sm_103a) DSA sparse-MLA library: Python binding of the C ABI.
+
+The three calls of the path -- ``topk_select``, ``sparse_mla_fwd`` and
+``combine`` -- marshal torch tensors (device memory, the current CUDA stream)
+into the C ABI declared in ``include/dsa.h`` and run entirely in the
+library's CUDA kernels.  There is no CPU or PyTorch fallback: if the library
+is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["DsaError", "load_library", "topk_select", "sparse_mla_fwd", "combine", "sparse_mla_topk",
+           "kv_tile_count", "kv_tile_size", "pick_num_splits", "status_string", "EXPORTED_SYMBOLS",
+           "DEV_BAD_QPOS", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsa.so")
+
+DEV_BAD_QPOS, DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4, 8
+
+# Every symbol include/dsa.h declares.
+EXPORTED_SYMBOLS = ("dsa_status_string", "dsa_version", "dsa_topk_select", "dsa_topk_workspace_size",
+                    "dsa_sparse_mla_fwd", "dsa_combine", "dsa_kv_tile_count", "dsa_kv_tile_size",
+                    "dsa_pick_num_splits")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def load_library(path: str | None = None):
+    """Load libdsa.so (built by ``__graft_entry__.build()`` or
+    ``python -m dsa_sparse_mla_topk_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                               "(python -m dsa_sparse_mla_topk_gb300.build)")
+        lib = ctypes.CDLL(p)
+        i32, i64, vp, f32, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+        lib.dsa_status_string.argtypes = [i32]
+        lib.dsa_status_string.restype = ctypes.c_char_p
+        lib.dsa_version.argtypes = []
+        lib.dsa_version.restype = i32
+        lib.dsa_topk_select.argtypes = [vp, i64, vp, i32, i32, vp, vp, sz, vp, vp]
+        lib.dsa_topk_select.restype = i32
+        lib.dsa_topk_workspace_size.argtypes = [i32, i64, i32]
+        lib.dsa_topk_workspace_size.restype = sz
+        lib.dsa_sparse_mla_fwd.argtypes = [vp, vp, vp, i64, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32,
+                                           f32, i32, vp, vp, vp, vp, vp, vp]
+        lib.dsa_sparse_mla_fwd.restype = i32
+        lib.dsa_combine.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
+        lib.dsa_combine.restype = i32
+        lib.dsa_kv_tile_count.argtypes = [i32, i32]
+        lib.dsa_kv_tile_count.restype = i32
+        lib.dsa_kv_tile_size.argtypes = [i32, i32, i32]
+        lib.dsa_kv_tile_size.restype = i32
+        lib.dsa_pick_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.dsa_pick_num_splits.restype = i32
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().dsa_status_string(int(status)).decode()
+
+
+def kv_tile_count(width: int, tile: int) -> int:
+    return load_library().dsa_kv_tile_count(int(width), int(tile))
+
+
+def kv_tile_size(heads: int, d_latent: int, d_rope: int) -> int:
+    return load_library().dsa_kv_tile_size(heads, d_latent, d_rope)
+
+
+def pick_num_splits(num_q: int, heads: int, d_latent: int, d_rope: int, k: int, num_sms: int = 0) -> int:
+    return load_library().dsa_pick_num_splits(num_q, heads, d_latent, d_rope, k, num_sms)
+
+
+def _p(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, ndim: int | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _call(fn: str, *args):
+    st = getattr(load_library(), fn)(*args)
+    if st != 0:
+        raise DsaError(fn, st)
+
+
+def topk_select(scores: torch.Tensor, q_pos: torch.Tensor, k: int, idx: torch.Tensor | None = None,
+                dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """int32 [num_q, k] causal top-k positions (ascending, -1 padded)."""
+    _check(scores, "scores", torch.float32, 2)
+    _check(q_pos, "q_pos", torch.int32, 1)
+    num_q, ld = scores.shape
+    if idx is None:
+        idx = torch.empty((num_q, k), dtype=torch.int32, device=scores.device)
+    _check(idx, "idx", torch.int32, 2)
+    ws_bytes = load_library().dsa_topk_workspace_size(num_q, ld, k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=scores.device) if ws_bytes else None
+    _call("dsa_topk_select", _p(scores), ld, _p(q_pos), num_q, k, _p(idx), _p(ws), ws_bytes, _p(dev_status),
+          _stream(stream))
+    return idx
+
+
+def sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, idx, *, d_latent: int, d_rope: int, page_size: int,
+                   softmax_scale: float, num_splits: int = 1, out=None, lse=None, o_part=None, lse_part=None,
+                   dev_status=None, stream=None):
+    """Partial step.  num_splits == 1: returns (out bf16, lse fp32).
+    num_splits > 1: returns (o_part fp32 [S, ...], lse_part fp32 [S, ...])."""
+    _check(q, "q", torch.bfloat16, 3)
+    _check(kv, "kv", torch.uint8, 2)
+    _check(kv_scale, "kv_scale", torch.float32, 1)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(q_req, "q_req", torch.int32, 1)
+    _check(idx, "idx", torch.int32, 2)
+    num_q, H, dqk = q.shape
+    if dqk != d_latent + d_rope or kv.shape[1] != dqk or kv.shape[0] % page_size:
+        raise ValueError("q / kv row sizes do not match d_latent + d_rope, or kv is not whole pages")
+    dev = q.device
+    if num_splits == 1:
+        if out is None:
+            out = torch.empty((num_q, H, d_latent), dtype=torch.bfloat16, device=dev)
+        if lse is None:
+            lse = torch.empty((num_q, H), dtype=torch.float32, device=dev)
+    else:
+        if o_part is None:
+            o_part = torch.empty((num_splits, num_q, H, d_latent), dtype=torch.float32, device=dev)
+        if lse_part is None:
+            lse_part = torch.empty((num_splits, num_q, H), dtype=torch.float32, device=dev)
+    _call("dsa_sparse_mla_fwd", _p(q), _p(kv), _p(kv_scale), kv.shape[0] // page_size, _p(block_table),
+          block_table.shape[0], block_table.shape[1], _p(q_req), _p(idx), num_q, H, d_latent, d_rope, page_size,
+          idx.shape[1], float(softmax_scale), num_splits, _p(out) if num_splits == 1 else None,
+          _p(lse) if num_splits == 1 else None, _p(o_part) if num_splits > 1 else None,
+          _p(lse_part) if num_splits > 1 else None, _p(dev_status), _stream(stream))
+    return (out, lse) if num_splits == 1 else (o_part, lse_part)
+
+
+def combine(o_part: torch.Tensor, lse_part: torch.Tensor, out=None, lse=None, stream=None):
+    """Combine step: (out bf16 [num_q, H, dv], lse fp32 [num_q, H])."""
+    _check(o_part, "o_part", torch.float32, 4)
+    _check(lse_part, "lse_part", torch.float32, 3)
+    S, num_q, H, dv = o_part.shape
+    if out is None:
+        out = torch.empty((num_q, H, dv), dtype=torch.bfloat16, device=o_part.device)
+    if lse is None:
+        lse = torch.empty((num_q, H), dtype=torch.float32, device=o_part.device)
+    _call("dsa_combine", _p(o_part), _p(lse_part), S, num_q, H, dv, _p(out), _p(lse), _stream(stream))
+    return out, lse
+
+
+def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, *, d_latent: int, d_rope: int,
+                    page_size: int, softmax_scale: float, num_splits: int | None = None, buffers: dict | None = None,
+                    dev_status=None, stream=None):
+    """One pass of the whole path: top-k -> Partial -> Combine (when split).
+    ``buffers`` (optional) holds preallocated idx / out / lse / o_part /
+    lse_part tensors.  Returns (out, lse, idx)."""
+    b = buffers or {}
+    num_q, H, _ = q.shape
+    if num_splits is None:
+        num_splits = pick_num_splits(num_q, H, d_latent, d_rope, k)
+    idx = topk_select(scores, q_pos, k, idx=b.get("idx"), dev_status=dev_status, stream=stream)
+    if num_splits == 1:
+        out, lse = sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, idx, d_latent=d_latent, d_rope=d_rope,
+                                  page_size=page_size, softmax_scale=softmax_scale, num_splits=1, out=b.get("out"),
+                                  lse=b.get("lse"), dev_status=dev_status, stream=stream)
+        return out, lse, idx
+    op, lp = sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, idx, d_latent=d_latent, d_rope=d_rope,
+                            page_size=page_size, softmax_scale=softmax_scale, num_splits=num_splits,
+                            o_part=b.get("o_part"), lse_part=b.get("lse_part"), dev_status=dev_status, stream=stream)
+    out, lse = combine(op, lp, out=b.get("out"), lse=b.get("lse"), stream=stream)
+    return out, lse, idx

@@ -1,0 +1,136 @@
+// C ABI of the library: argument checks, planning helpers and launches.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "dsa.h"
+#include "internal.cuh"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_shape(int32_t h, int32_t dl, int32_t dr) {
+  return (h == 16 && dl == 64 && dr == 16) || (h == 64 && dl == 512 && dr == 64);
+}
+
+dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(int32_t status) {
+  switch (status) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED_SHAPE: return "unsupported (heads, d_latent, d_rope)";
+    case DSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case DSA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int32_t dsa_version(void) { return 100; }
+
+int32_t dsa_kv_tile_count(int32_t width, int32_t tile) {
+  if (width < 0 || tile <= 0) return -1;
+  return (int32_t)(((int64_t)width + tile - 1) / tile);
+}
+
+int32_t dsa_kv_tile_size(int32_t num_heads, int32_t d_latent, int32_t d_rope) {
+  if (!supported_shape(num_heads, d_latent, d_rope)) return -1;
+  return 32;
+}
+
+int32_t dsa_pick_num_splits(int32_t num_q, int32_t num_heads, int32_t d_latent, int32_t d_rope, int32_t k,
+                            int32_t num_sms) {
+  const int32_t tile = dsa_kv_tile_size(num_heads, d_latent, d_rope);
+  if (tile <= 0 || num_q <= 0 || k <= 0) return 1;
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 148;
+  }
+  // query tokens alone fill the GPU: no split (no partials, no combine)
+  if (num_q >= num_sms) return 1;
+  const int32_t ntiles = dsa_kv_tile_count(k, tile);
+  int32_t s = (2 * num_sms + num_q - 1) / num_q;  // about two CTAs per SM
+  if (s > ntiles) s = ntiles;
+  if (s > 64) s = 64;
+  return s < 1 ? 1 : s;
+}
+
+size_t dsa_topk_workspace_size(int32_t num_q, int64_t ld_scores, int32_t k) {
+  (void)num_q, (void)ld_scores, (void)k;
+  return 0;
+}
+
+dsa_status dsa_topk_select(const float* scores, int64_t ld_scores, const int32_t* q_pos, int32_t num_q,
+                           int32_t k, int32_t* idx, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream) {
+  if (num_q < 0 || k <= 0 || ld_scores <= 0) return DSA_ERR_INVALID_ARG;
+  if (num_q == 0) return DSA_OK;
+  if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
+  if (workspace_bytes < dsa_topk_workspace_size(num_q, ld_scores, k)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  (void)workspace;
+  return from_cuda(dsa::launch_topk_radix(scores, ld_scores, q_pos, num_q, k, idx, dev_status,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_scale, int64_t num_pages,
+                              const int32_t* block_table, int32_t num_req, int32_t bt_stride,
+                              const int32_t* q_req, const int32_t* idx, int32_t num_q, int32_t num_heads,
+                              int32_t d_latent, int32_t d_rope, int32_t page_size, int32_t k,
+                              float softmax_scale, int32_t num_splits, void* out, float* lse, float* o_part,
+                              float* lse_part, int32_t* dev_status, void* stream) {
+  if (num_q < 0 || k <= 0 || page_size <= 0 || num_pages <= 0 || num_req <= 0 || bt_stride <= 0)
+    return DSA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 64 || !isfinite(softmax_scale)) return DSA_ERR_INVALID_ARG;
+  if (!supported_shape(num_heads, d_latent, d_rope)) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (num_q == 0) return DSA_OK;
+  if (!q || !kv || !kv_scale || !block_table || !q_req || !idx) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
+  if (num_splits == 1) {
+    if (!out) return DSA_ERR_INVALID_ARG;
+  } else {
+    if (!o_part || !lse_part || !aligned16(o_part)) return DSA_ERR_INVALID_ARG;
+  }
+  dsa::MlaArgs a;
+  a.q = q;
+  a.kv = kv;
+  a.kv_scale = kv_scale;
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  a.num_req = num_req;
+  a.bt_stride = bt_stride;
+  a.q_req = q_req;
+  a.idx = idx;
+  a.num_q = num_q;
+  a.heads = num_heads;
+  a.d_latent = d_latent;
+  a.d_rope = d_rope;
+  a.page_size = page_size;
+  a.k = k;
+  a.softmax_scale = softmax_scale;
+  a.num_splits = num_splits;
+  a.out = out;
+  a.lse = lse;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.dev_status = dev_status;
+  return from_cuda(dsa::launch_mla_simt(a, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t num_q,
+                       int32_t num_heads, int32_t d_v, void* out, float* lse, void* stream) {
+  if (num_q < 0 || num_splits < 1 || num_splits > 64 || num_heads < 1 || num_heads > 64 || d_v <= 0 ||
+      d_v % 4 != 0)
+    return DSA_ERR_INVALID_ARG;
+  if (num_q == 0) return DSA_OK;
+  if (!o_part || !lse_part || !out || !aligned16(o_part) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+  return from_cuda(dsa::launch_combine(o_part, lse_part, num_splits, num_q, num_heads, d_v, out, lse,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

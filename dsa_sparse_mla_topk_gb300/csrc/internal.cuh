@@ -1,0 +1,45 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+// Kernel launchers (each returns the launch's cudaError_t).
+cudaError_t launch_topk_radix(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
+                              int32_t* idx, int32_t* dev_status, cudaStream_t stream);
+
+struct MlaArgs {
+  const void* q;
+  const uint8_t* kv;
+  const float* kv_scale;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int32_t num_req;
+  int32_t bt_stride;
+  const int32_t* q_req;
+  const int32_t* idx;
+  int32_t num_q, heads, d_latent, d_rope, page_size, k;
+  float softmax_scale;
+  int32_t num_splits;
+  void* out;
+  float* lse;
+  float* o_part;
+  float* lse_part;
+  int32_t* dev_status;
+};
+
+cudaError_t launch_mla_simt(const MlaArgs& a, cudaStream_t stream);
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t num_q,
+                           int32_t heads, int32_t d_v, void* out, float* lse, cudaStream_t stream);
+
+// Report a data-dependent error without trapping.
+__device__ __forceinline__ void report(int32_t* status, uint32_t bit) {
+  if (status) atomicOr(reinterpret_cast<unsigned int*>(status), bit);
+}
+
+}  // namespace dsa

@@ -1,0 +1,183 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DSA sparse-MLA library.
+ *
+ * The library implements the data-parallel hot path of DeepSeek-style sparse
+ * attention (DSA) over multi-head latent attention (MLA) with an FP8 paged KV
+ * cache, as described for GLM-5.3-Flash serving:
+ *
+ *   scores --dsa_topk_select--> idx --dsa_sparse_mla_fwd--> (out, lse)
+ *                                              \--(splits)--> partials --dsa_combine--> (out, lse)
+ *
+ * Sources (page titles):
+ *  [LMSYS]  "Accelerating GLM-5.3-Flash on H200: High-Throughput Disaggregated
+ *           Serving": section 1 "Architecture and workloads" (an indexer picks
+ *           historical positions, DSA attends to them), section 2 "KV-only
+ *           decode RadixCache" (prefix KV pages shared across requests),
+ *           section 3 "Larger KV tiles for DSA Partial" and Figure 4 (the
+ *           Partial step computes QK^T, online softmax and the weighted value
+ *           sum over the selected positions; KV splits need a Combine step).
+ *  [vLLM]   "GLM-5.3 Optimizations, Part 2: PCP, DCP, and Hybrid HiSparse on
+ *           16 H200s", "Interpretation" (MLA's latent KV row is shared by all
+ *           64 heads).
+ *  [SGLang] GLM-5.3-Flash cookbook, "Size both memory pools" (paged KV pool)
+ *           and "Keep the KV and DSA backends paired" (FP8 E4M3 KV cache on
+ *           Blackwell).
+ *
+ * Conventions shared by every entry point:
+ *  - All pointers except those documented as host pointers are DEVICE
+ *    pointers.  The caller owns every buffer; the library allocates no device
+ *    memory, keeps no per-call state and is reentrant.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously; the call returns after argument checks and
+ *    kernel launch.
+ *  - Argument errors are reported synchronously through the return value and
+ *    nothing is launched.  A failed launch returns DSA_ERR_CUDA.
+ *  - Data-dependent errors (an index or page id out of range, a bad query
+ *    position, an expired wait) never trap the GPU: the kernel ORs a bit
+ *    (DSA_DEV_*) into `*dev_status` (an int32 in device memory, may be NULL)
+ *    and the offending row contributes nothing.
+ *  - Supported (heads, d_latent, d_rope): (16, 64, 16) and (64, 512, 64).
+ *    A KV row is d_latent + d_rope FP8 E4M3 bytes (a multiple of 16) with one
+ *    fp32 scale per token; K is the whole row, V its first d_latent bytes.
+ */
+#ifndef DSA_SPARSE_MLA_H_
+#define DSA_SPARSE_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad alignment */
+  DSA_ERR_UNSUPPORTED_SHAPE = 2, /* (heads, d_latent, d_rope) not compiled in */
+  DSA_ERR_WORKSPACE_TOO_SMALL = 3,
+  DSA_ERR_CUDA = 4 /* a CUDA runtime call or kernel launch failed */
+} dsa_status;
+
+/* Bits ORed into *dev_status by the kernels. */
+#define DSA_DEV_BAD_QPOS 1u  /* q_pos[i] < 0 or >= ld_scores: the row selects nothing */
+#define DSA_DEV_BAD_INDEX 2u /* idx entry < -1, or its page slot is past the block table row */
+#define DSA_DEV_BAD_PAGE 4u  /* block table entry < 0 or >= num_pages, or q_req out of range */
+#define DSA_DEV_TIMEOUT 8u   /* a bounded wait inside a kernel expired */
+
+/* Static description of a status code (never NULL). */
+DSA_API const char* dsa_status_string(int32_t status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+DSA_API int32_t dsa_version(void);
+
+/*
+ * dsa_topk_select -- causal top-k over fp32 indexer scores.
+ * [LMSYS] section 3: "the indexer selects KV positions" that the Partial step
+ * then loads; [LMSYS] section 1: the indexer picks relevant historical
+ * positions.
+ *
+ * For each query row i (0 <= i < num_q) the visible positions are
+ * 0..q_pos[i] (causal).  The call writes idx[i, 0:k] (int32, row-major,
+ * device) = the min(k, q_pos[i] + 1) visible positions with the largest
+ * scores[i, :], ranked by (score descending, position ascending) -- equal
+ * scores go to the lower position and -0.0 equals +0.0 -- listed in
+ * ascending position order, followed by -1 padding.  NaN scores are not
+ * allowed (the result is unspecified but stays in range).
+ *
+ *   scores     fp32 [num_q, ld_scores], row stride ld_scores elements.
+ *   q_pos      int32 [num_q]; q_pos[i] must lie in [0, ld_scores).
+ *   idx        int32 [num_q, k] output.
+ *   workspace  device scratch of at least dsa_topk_workspace_size() bytes
+ *              (may be NULL when that size is 0).
+ * Errors: num_q < 0, k <= 0, ld_scores <= 0, null pointers -> INVALID_ARG;
+ * q_pos out of range -> dev bit DSA_DEV_BAD_QPOS and a row of -1.
+ */
+DSA_API dsa_status dsa_topk_select(const float* scores, int64_t ld_scores, const int32_t* q_pos, int32_t num_q,
+                           int32_t k, int32_t* idx, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream);
+
+/* Scratch bytes dsa_topk_select needs for these sizes. */
+DSA_API size_t dsa_topk_workspace_size(int32_t num_q, int64_t ld_scores, int32_t k);
+
+/*
+ * dsa_sparse_mla_fwd -- the DSA "Partial" step: sparse MLA attention of every
+ * head of each query token over its selected latent-KV rows.
+ * [LMSYS] section 3 "Larger KV tiles for DSA Partial": loads the selected KV
+ * positions and computes QK^T, online softmax and the weighted value sum;
+ * [vLLM] "Interpretation": one latent KV row serves all heads; [SGLang]: FP8
+ * E4M3 paged KV.
+ *
+ * For query token i, request r = q_req[i], head h and every selected
+ * position p = idx[i, j] != -1:
+ *   slot  = block_table[r * bt_stride + p / page_size] * page_size + p % page_size
+ *   x_d   = e4m3(kv[slot, d]) * kv_scale[slot]                 (d < dqk)
+ *   z_p   = softmax_scale * sum_d q[i, h, d] * x_d
+ *   out[i, h, :] = sum_p softmax(z)_p * x[:d_latent],   lse[i, h] = ln sum_p exp(z_p)
+ * A token with no selected rows gets out = 0 and lse = -inf.
+ *
+ *   q            bf16 [num_q, heads, dqk] (dqk = d_latent + d_rope), 16-byte aligned.
+ *   kv           e4m3 bytes [num_pages * page_size, dqk], 16-byte aligned.
+ *   kv_scale     fp32 [num_pages * page_size].
+ *   block_table  int32 [num_req, bt_stride] page ids; rows may share pages.
+ *   q_req        int32 [num_q] request of each query token, in [0, num_req).
+ *   idx          int32 [num_q, k] selected positions (-1 = none), any order.
+ *   num_splits   1..64.  With 1 the call writes out (bf16 [num_q, heads,
+ *                d_latent]) and lse (fp32 [num_q, heads]).  With S > 1 the k
+ *                entries of each row are cut into S contiguous chunks of whole
+ *                KV tiles and the call writes o_part (fp32 [S, num_q, heads,
+ *                d_latent]) and lse_part (fp32 [S, num_q, heads]) instead, to
+ *                be merged by dsa_combine; out and lse may then be NULL.
+ * Errors: see the conventions above; page ids or indices out of range set
+ * DSA_DEV_BAD_INDEX / DSA_DEV_BAD_PAGE and that row is skipped.
+ */
+DSA_API dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_scale, int64_t num_pages,
+                              const int32_t* block_table, int32_t num_req, int32_t bt_stride,
+                              const int32_t* q_req, const int32_t* idx, int32_t num_q, int32_t num_heads,
+                              int32_t d_latent, int32_t d_rope, int32_t page_size, int32_t k,
+                              float softmax_scale, int32_t num_splits, void* out, float* lse, float* o_part,
+                              float* lse_part, int32_t* dev_status, void* stream);
+
+/*
+ * dsa_combine -- the DSA "Combine" step: exact log-sum-exp merge of split-KV
+ * partial results.  [LMSYS] section 3: KV splits add intermediate writes and
+ * Combine work.
+ *   lse[i, h] = ln sum_s exp(lse_part[s, i, h])
+ *   out[i, h, :] = sum_s exp(lse_part[s, i, h] - lse[i, h]) * o_part[s, i, h, :]
+ * Splits with lse_part = -inf are empty and ignored; if all are, out = 0 and
+ * lse = -inf.  o_part fp32 [S, num_q, heads, d_v]; lse_part fp32 [S, num_q,
+ * heads]; out bf16 [num_q, heads, d_v]; lse fp32 [num_q, heads] (may be NULL).
+ * d_v must be a multiple of 4 and o_part 16-byte aligned.
+ */
+DSA_API dsa_status dsa_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t num_q,
+                       int32_t num_heads, int32_t d_v, void* out, float* lse, void* stream);
+
+/*
+ * Host-side planning helpers (no GPU needed).
+ *
+ * dsa_kv_tile_count: KV tiles of `tile` entries that cover an index row of
+ * `width` entries; the last tile is padded virtually, the index tensor is
+ * unchanged ([LMSYS] Figure 4: width 2112 -> 66 tiles of 32 or 17 of 128,
+ * 2176 virtual columns of which 64 are padding).
+ *
+ * dsa_pick_num_splits: KV splits per query token for the given launch.  KV
+ * splits are added only while query tokens alone leave SMs idle ([LMSYS]
+ * section 3: splits cost intermediate writes and Combine work, so they are
+ * used only when query parallelism is insufficient).  num_sms <= 0 queries
+ * the current device.
+ */
+DSA_API int32_t dsa_kv_tile_count(int32_t width, int32_t tile);
+DSA_API int32_t dsa_kv_tile_size(int32_t num_heads, int32_t d_latent, int32_t d_rope);
+DSA_API int32_t dsa_pick_num_splits(int32_t num_q, int32_t num_heads, int32_t d_latent, int32_t d_rope, int32_t k,
+                            int32_t num_sms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_SPARSE_MLA_H_ */

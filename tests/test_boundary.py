@@ -1,0 +1,133 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+symbol, validates arguments before touching the device, and its host-side
+planning helpers follow the tiling arithmetic of the pages."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dsa_sparse_mla_topk_gb300 as dsa
+from dsa_sparse_mla_topk_gb300 import build as dsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dsa_build.build()
+    return dsa.load_library()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(dsa.EXPORTED_SYMBOLS) == _declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert dsa.status_string(0) == "ok"
+    for s in range(1, 5):
+        assert dsa.status_string(s) not in ("ok", "unknown status")
+    assert dsa.status_string(99) == "unknown status"
+    assert lib.dsa_version() >= 100
+
+
+def test_tile_count_worked_example(lib):
+    """"Accelerating GLM-5.3-Flash on H200", Figure 4: an index width of 2112
+    takes 66 tiles of 32 or 17 tiles of 128; the 128-wide tiles cover 2176
+    virtual columns of which the last 64 are padding."""
+    assert dsa.kv_tile_count(2112, 32) == 66
+    assert dsa.kv_tile_count(2112, 128) == 17
+    assert dsa.kv_tile_count(2112, 128) * 128 == 2176
+    assert dsa.kv_tile_count(2112, 128) * 128 - 2112 == 64
+    assert dsa.kv_tile_count(0, 64) == 0
+    assert dsa.kv_tile_count(5, 0) == -1
+
+
+def test_split_rule(lib):
+    """Splits only when query tokens alone leave SMs idle; never more splits
+    than KV tiles."""
+    tile = dsa.kv_tile_size(64, 512, 64)
+    assert tile > 0 and dsa.kv_tile_size(32, 512, 64) == -1
+    assert dsa.pick_num_splits(32768, 64, 512, 64, 2048, num_sms=152) == 1
+    assert dsa.pick_num_splits(1024, 64, 512, 64, 2048, num_sms=152) == 1
+    s_dec = dsa.pick_num_splits(128, 64, 512, 64, 2048, num_sms=152)
+    assert 1 < s_dec <= dsa.kv_tile_count(2048, tile)
+    s_1m = dsa.pick_num_splits(16, 64, 512, 64, 2048, num_sms=152)
+    assert s_1m >= s_dec
+    assert dsa.pick_num_splits(2, 16, 64, 16, 64, num_sms=152) <= dsa.kv_tile_count(64, dsa.kv_tile_size(16, 64, 16))
+
+
+# ---- argument validation: every case returns before any CUDA call ----
+
+VP = ctypes.c_void_p
+FAKE = VP(0x10000)  # 16-byte aligned, never dereferenced on these paths
+MISALIGNED = VP(0x10004)
+
+
+def _fwd(lib, **over):
+    a = dict(q=FAKE, kv=FAKE, kv_scale=FAKE, num_pages=4, bt=FAKE, num_req=1, bt_stride=4, q_req=FAKE, idx=FAKE,
+             num_q=1, H=64, dl=512, dr=64, P=64, k=2048, scale=0.04, S=1, out=FAKE, lse=FAKE, op=None, lp=None,
+             st=None, stream=None)
+    a.update(over)
+    return lib.dsa_sparse_mla_fwd(a["q"], a["kv"], a["kv_scale"], a["num_pages"], a["bt"], a["num_req"],
+                                  a["bt_stride"], a["q_req"], a["idx"], a["num_q"], a["H"], a["dl"], a["dr"], a["P"],
+                                  a["k"], a["scale"], a["S"], a["out"], a["lse"], a["op"], a["lp"], a["st"],
+                                  a["stream"])
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(H=32), 2), (dict(dl=256), 2), (dict(dr=32), 2),
+    (dict(k=0), 1), (dict(P=0), 1), (dict(num_q=-1), 1), (dict(S=0), 1), (dict(S=65), 1),
+    (dict(q=None), 1), (dict(kv=None), 1), (dict(idx=None), 1), (dict(out=None), 1),
+    (dict(q=MISALIGNED), 1), (dict(kv=MISALIGNED), 1), (dict(scale=float("inf")), 1),
+    (dict(S=4, op=None, lp=FAKE), 1), (dict(S=4, op=MISALIGNED, lp=FAKE), 1), (dict(num_pages=0), 1),
+    (dict(num_q=0), 0),
+])
+def test_fwd_argument_checks(lib, over, expect):
+    assert _fwd(lib, **over) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, 100, FAKE, 4, 0, FAKE, None, 0, None, None), 1),
+    ((FAKE, 0, FAKE, 4, 8, FAKE, None, 0, None, None), 1),
+    ((None, 100, FAKE, 4, 8, FAKE, None, 0, None, None), 1),
+    ((FAKE, 100, None, 4, 8, FAKE, None, 0, None, None), 1),
+    ((FAKE, 100, FAKE, 4, 8, None, None, 0, None, None), 1),
+    ((FAKE, 100, FAKE, -1, 8, FAKE, None, 0, None, None), 1),
+    ((FAKE, 100, FAKE, 0, 8, FAKE, None, 0, None, None), 0),
+])
+def test_topk_argument_checks(lib, args, expect):
+    assert lib.dsa_topk_select(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, FAKE, 0, 4, 64, 512, FAKE, FAKE, None), 1),
+    ((FAKE, FAKE, 65, 4, 64, 512, FAKE, FAKE, None), 1),
+    ((FAKE, FAKE, 2, 4, 65, 512, FAKE, FAKE, None), 1),
+    ((FAKE, FAKE, 2, 4, 64, 510, FAKE, FAKE, None), 1),
+    ((None, FAKE, 2, 4, 64, 512, FAKE, FAKE, None), 1),
+    ((MISALIGNED, FAKE, 2, 4, 64, 512, FAKE, FAKE, None), 1),
+    ((FAKE, FAKE, 2, 0, 64, 512, FAKE, FAKE, None), 0),
+])
+def test_combine_argument_checks(lib, args, expect):
+    assert lib.dsa_combine(*args) == expect
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        dsa.topk_select(torch.zeros(2, 8), torch.zeros(2, dtype=torch.int32), 4)
+    with pytest.raises(TypeError):
+        dsa.topk_select(torch.zeros(2, 8, dtype=torch.float64), torch.zeros(2, dtype=torch.int32), 4)

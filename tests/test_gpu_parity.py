@@ -1,0 +1,253 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Top-k indices must match bit for bit.  Attention outputs must lie within
+max-abs 1e-2 and relative L2 5e-3 of the oracle's fp64 result on the same
+(dequantised) inputs; LSE within 1e-3 absolute.  Full-size workloads are run
+in the launch configuration the benchmark times and checked on sampled query
+tokens that the oracle computes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dsa_sparse_mla_topk_gb300 as dsa
+from dsa_sparse_mla_topk_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, REL_L2, LSE_ABS = 1e-2, 5e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dsa_sparse_mla_topk_gb300 import build
+    build.build()
+    dsa.load_library()
+
+
+_CACHE = {}
+
+
+def inputs(w: wl.Workload):
+    if w.name not in _CACHE:
+        _CACHE.clear()
+        torch.cuda.empty_cache()
+        _CACHE[w.name] = wl.make_inputs(w, device="cuda")
+    return _CACHE[w.name]
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def run(inp, num_splits=None, status=None):
+    w = inp.w
+    out, lse, idx = dsa.sparse_mla_topk(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, inp.q_pos,
+                                        inp.scores, w.k, d_latent=w.d_latent, d_rope=w.d_rope,
+                                        page_size=w.page_size, softmax_scale=w.scale, num_splits=num_splits,
+                                        dev_status=status)
+    torch.cuda.synchronize()
+    return out, lse, idx
+
+
+def oracle_rows(inp, rows):
+    """Oracle top-k and attention for the given query tokens."""
+    w = inp.w
+    rows = np.asarray(rows)
+    rt = torch.as_tensor(rows, device=inp.scores.device)
+    scores = host(inp.scores.index_select(0, rt))
+    q_pos = host(inp.q_pos)[rows]
+    idx = oracle.topk(scores, q_pos, w.k)
+    out, lse = oracle.sparse_mla(host(inp.q.index_select(0, rt).view(torch.int16)), host(inp.kv), host(inp.kv_scale),
+                                 host(inp.block_table), host(inp.q_req)[rows], idx, d_latent=w.d_latent,
+                                 d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+    return idx, out, lse
+
+
+def assert_close(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
+    a = out_gpu.astype(np.float64)
+    err = np.abs(a - out_ref)
+    max_abs = float(err.max()) if err.size else 0.0
+    rel = float(np.linalg.norm(a - out_ref) / max(np.linalg.norm(out_ref), 1e-300))
+    assert max_abs <= MAX_ABS, f"{what}: max-abs {max_abs:.3e}"
+    assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3e}"
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(fin, np.isfinite(lse_gpu)), f"{what}: lse finiteness differs"
+    if fin.any():
+        d = float(np.abs(lse_gpu[fin] - lse_ref[fin]).max())
+        assert d <= LSE_ABS, f"{what}: lse max-abs {d:.3e}"
+    return max_abs, rel
+
+
+def sample_rows(n, m, seed=0):
+    if n <= m:
+        return np.arange(n)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, n - 1), size=m - 2, replace=False)
+    return np.sort(np.concatenate([[0, n - 1], mid]))
+
+
+SMALL_H64 = wl.Workload("small_h64_ragged", 3, 3, 64, 512, 64, 3000, 0, 64, 2048, seed=21,
+                        ctx_per_req=(3000, 2101, 700))
+SMALL_H16 = wl.Workload("small_h16_ragged_prefix", 4, 2, 16, 64, 16, 1000, 333, 16, 64, seed=22,
+                        ctx_per_req=(1000, 900, 334, 345), tie_frac=0.05)
+
+FULL = [(wl.TINY, None), (SMALL_H16, None), (SMALL_H64, None), (wl.DECODE_64K, 128), (wl.VERIFY_64K, 96),
+        (wl.PREFILL_32K, 40), (wl.CTX_1M, 16)]
+
+
+@pytest.mark.parametrize("w,nsample", FULL, ids=[w.name for w, _ in FULL])
+def test_path_matches_oracle(w, nsample):
+    inp = inputs(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse, idx = run(inp, status=status)
+    assert int(status.item()) == 0
+    rows = np.arange(w.num_q) if nsample is None else sample_rows(w.num_q, nsample)
+    ref_idx, ref_out, ref_lse = oracle_rows(inp, rows)
+    got_idx = host(idx)[rows]
+    assert np.array_equal(got_idx, ref_idx), "top-k indices differ from the oracle"
+    assert_close(host(out.float())[rows], host(lse)[rows], ref_out, ref_lse, w.name)
+
+
+@pytest.mark.parametrize("w", [wl.DECODE_64K, wl.VERIFY_64K, wl.CTX_1M], ids=lambda w: w.name)
+def test_topk_whole_index_array_bit_exact(w):
+    inp = inputs(w)
+    idx = dsa.topk_select(inp.scores, inp.q_pos, w.k)
+    torch.cuda.synchronize()
+    ref = oracle.topk(host(inp.scores), host(inp.q_pos), w.k)
+    assert np.array_equal(host(idx), ref)
+
+
+def test_topk_prefill_rows_bit_exact_sampled():
+    w = wl.PREFILL_32K
+    inp = inputs(w)
+    idx = dsa.topk_select(inp.scores, inp.q_pos, w.k)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.num_q, 256, seed=5)
+    rt = torch.as_tensor(rows, device="cuda")
+    ref = oracle.topk(host(inp.scores.index_select(0, rt)), host(inp.q_pos)[rows], w.k)
+    assert np.array_equal(host(idx)[rows], ref)
+    # every row: ascending, unique, in range
+    i = idx.long()
+    assert bool((i[:, 1:] > i[:, :-1]).all())
+    assert bool((i >= 0).all()) and bool((i <= inp.q_pos.long()[:, None]).all())
+
+
+@pytest.mark.parametrize("w", [wl.TINY, SMALL_H64], ids=lambda w: w.name)
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_split_count_invariance(w, splits):
+    inp = inputs(w)
+    out1, lse1, _ = run(inp, num_splits=1)
+    outS, lseS, _ = run(inp, num_splits=splits)
+    d = (out1.float() - outS.float()).abs().max().item()
+    assert d <= 4e-3
+    fin = torch.isfinite(lse1)
+    assert torch.equal(fin, torch.isfinite(lseS))
+    assert (lse1[fin] - lseS[fin]).abs().max().item() <= 1e-4
+
+
+def test_combine_matches_oracle_merge():
+    w = SMALL_H64
+    inp = inputs(w)
+    idx = dsa.topk_select(inp.scores, inp.q_pos, w.k)
+    op, lp = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, d_latent=w.d_latent,
+                                d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale, num_splits=5)
+    out, lse = dsa.combine(op, lp)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.combine(host(op).astype(np.float64), host(lp).astype(np.float64))
+    np.testing.assert_allclose(host(out.float()), ref_out, rtol=0, atol=8e-3 * np.abs(ref_out).max() + 1e-6)
+    np.testing.assert_allclose(host(lse), ref_lse, rtol=0, atol=1e-5)
+
+
+def test_golden_ties_on_gpu():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "topk_ties.txt")
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, qp, k, sc, exp = [t.strip() for t in line.split("|")]
+        scores = torch.tensor([[float(v) for v in sc.split(",")]], dtype=torch.float32, device="cuda")
+        idx = dsa.topk_select(scores, torch.tensor([int(qp)], dtype=torch.int32, device="cuda"), int(k))
+        assert host(idx)[0].tolist() == [int(v) for v in exp.split(",")], name
+
+
+def test_topk_long_ties_and_ragged_lengths():
+    """Rows of heavily tied integer scores, unaligned lengths and k near the
+    visible count (exercises every radix pass and the tie cut)."""
+    rng = np.random.default_rng(9)
+    n, ld, k = 40, 9001, 777
+    scores = rng.integers(-3, 4, size=(n, ld)).astype(np.float32)
+    scores[rng.random((n, ld)) < 0.05] = -0.0
+    q_pos = np.concatenate([rng.integers(0, ld, size=n - 4), [ld - 1, k - 1, k, 0]]).astype(np.int32)
+    got = dsa.topk_select(torch.tensor(scores, device="cuda"), torch.tensor(q_pos, device="cuda"), k)
+    assert np.array_equal(host(got), oracle.topk(scores, q_pos, k))
+    # odd row stride (unaligned rows)
+    sc2 = torch.tensor(rng.standard_normal((8, 4099)).astype(np.float32), device="cuda")
+    qp2 = torch.tensor([4098, 4000, 3000, 2048, 2047, 100, 4097, 1], dtype=torch.int32, device="cuda")
+    got2 = dsa.topk_select(sc2, qp2, 2048)
+    assert np.array_equal(host(got2), oracle.topk(host(sc2), host(qp2), 2048))
+
+
+def test_bad_inputs_set_status_without_faulting():
+    w = wl.TINY
+    inp = inputs(w)
+    # q_pos out of range -> row of -1 and BAD_QPOS
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qp = inp.q_pos.clone()
+    qp[0] = inp.scores.shape[1] + 5
+    idx = dsa.topk_select(inp.scores, qp, w.k, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & dsa.DEV_BAD_QPOS and bool((idx[0] == -1).all())
+    # index below -1 and a position past the block table -> BAD_INDEX; page id out of range -> BAD_PAGE
+    idx = dsa.topk_select(inp.scores, inp.q_pos, w.k)
+    bad = idx.clone()
+    bad[0, 0] = -7
+    bad[1, 0] = 10 ** 6
+    st.zero_()
+    out, lse = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, bad, d_latent=w.d_latent,
+                                  d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & dsa.DEV_BAD_INDEX
+    bt = inp.block_table.clone()
+    bt[0, 0] = 10 ** 6
+    st.zero_()
+    dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, bt, inp.q_req, idx, d_latent=w.d_latent, d_rope=w.d_rope,
+                       page_size=w.page_size, softmax_scale=w.scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & dsa.DEV_BAD_PAGE
+    assert torch.isfinite(out.float()).all()
+
+
+def test_empty_selection_gives_zero_and_minus_inf():
+    w = SMALL_H64
+    inp = inputs(w)
+    idx = torch.full((w.num_q, w.k), -1, dtype=torch.int32, device="cuda")
+    for s in (1, 4):
+        if s == 1:
+            out, lse = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx,
+                                          d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size,
+                                          softmax_scale=w.scale)
+        else:
+            op, lp = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx,
+                                        d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size,
+                                        softmax_scale=w.scale, num_splits=s)
+            out, lse = dsa.combine(op, lp)
+        torch.cuda.synchronize()
+        assert bool((out == 0).all()) and bool(torch.isneginf(lse).all())
+
+
+def test_permuted_indices_give_same_output():
+    w = SMALL_H64
+    inp = inputs(w)
+    idx = dsa.topk_select(inp.scores, inp.q_pos, w.k)
+    perm = torch.argsort(torch.rand(idx.shape, device="cuda"), dim=1)
+    idx2 = torch.gather(idx, 1, perm).contiguous()
+    kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+    o1, l1 = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, **kw)
+    o2, l2 = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx2, **kw)
+    torch.cuda.synchronize()
+    assert (o1.float() - o2.float()).abs().max().item() <= 4e-3
