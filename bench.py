@@ -384,7 +384,8 @@ def bench_ours(args):
 
     peaks = read_peaks()
     fwd_ms = statistics.mean(t_fwd)
-    src = os.path.join(ROOT, "dsa_sparse_mla_topk_gb300", "csrc", "mla_simt.cu")
+    src = os.path.join(ROOT, "dsa_sparse_mla_topk_gb300", "csrc",
+                       "mla_tc.cu" if w.heads == 64 and os.environ.get("DSA_FORCE_SIMT") != "1" else "mla_simt.cu")
     sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
     tr = TRAFFIC_BY_SOURCE.get(sha)
     traffic = None
@@ -409,7 +410,7 @@ def bench_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp32", "data": "synthetic (seeded; shapes of the GLM-5.3-Flash workloads)",
+            "vs_baseline": None, "dtype": "bf16" if src.endswith("mla_tc.cu") else "fp32", "data": "synthetic (seeded; shapes of the GLM-5.3-Flash workloads)",
             "config": workload_config(w, S, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
             "roofline": {"kernel": "sparse_mla_fwd", "bound": "hbm", "achieved": achieved_gbs,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],

@@ -1,6 +1,7 @@
 // C ABI of the library: argument checks, planning helpers and launches.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include "dsa.h"
 #include "internal.cuh"
@@ -39,7 +40,7 @@ int32_t dsa_kv_tile_count(int32_t width, int32_t tile) {
 
 int32_t dsa_kv_tile_size(int32_t num_heads, int32_t d_latent, int32_t d_rope) {
   if (!supported_shape(num_heads, d_latent, d_rope)) return -1;
-  return 32;
+  return num_heads == 64 ? 128 : 32;  // tensor-core kernel: 128-row tiles; CUDA-core kernel: 32
 }
 
 int32_t dsa_pick_num_splits(int32_t num_q, int32_t num_heads, int32_t d_latent, int32_t d_rope, int32_t k,
@@ -54,11 +55,19 @@ int32_t dsa_pick_num_splits(int32_t num_q, int32_t num_heads, int32_t d_latent, 
   }
   // query tokens alone fill the GPU: no split (no partials, no combine)
   if (num_q >= num_sms) return 1;
+  // One CTA per SM (shared memory bound); a launch takes ceil(CTAs / SMs)
+  // waves of ceil(tiles / S) tiles each, plus a fixed per-CTA cost (start-up,
+  // epilogue) of about two tiles and one more for the Combine when split.
   const int32_t ntiles = dsa_kv_tile_count(k, tile);
-  int32_t s = (2 * num_sms + num_q - 1) / num_q;  // about two CTAs per SM
-  if (s > ntiles) s = ntiles;
-  if (s > 64) s = 64;
-  return s < 1 ? 1 : s;
+  int32_t best = 1;
+  int64_t best_cost = -1;
+  for (int32_t s = 1; s <= 64 && s <= ntiles; ++s) {
+    const int64_t waves = ((int64_t)num_q * s + num_sms - 1) / num_sms;
+    const int64_t per = (ntiles + s - 1) / s;
+    const int64_t cost = waves * (per + 2) + (s > 1 ? 1 : 0);
+    if (best_cost < 0 || cost < best_cost) best = s, best_cost = cost;
+  }
+  return best;
 }
 
 size_t dsa_topk_workspace_size(int32_t num_q, int64_t ld_scores, int32_t k) {
@@ -119,6 +128,9 @@ dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_
   a.o_part = o_part;
   a.lse_part = lse_part;
   a.dev_status = dev_status;
+  const char* force = getenv("DSA_FORCE_SIMT");
+  const bool simt = force && force[0] == '1';
+  if (!simt && dsa::mla_tc_supported(a)) return from_cuda(dsa::launch_mla_tc(a, static_cast<cudaStream_t>(stream)));
   return from_cuda(dsa::launch_mla_simt(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -1,0 +1,617 @@
+// Sparse MLA attention on the Blackwell tensor cores (tcgen05 + TMEM).
+//
+// "Accelerating GLM-5.3-Flash on H200", section 3 "Larger KV tiles for DSA
+// Partial": the Partial step loads the KV positions the indexer selected and
+// computes Q K^T, an online softmax and the weighted value sum, one KV tile at
+// a time (Figure 4: the last tile is padded virtually, the index tensor is
+// left alone); a KV split writes a partial result for the Combine step.
+// "GLM-5.3 Optimizations, Part 2" ("Interpretation"): every latent KV row is
+// shared by all 64 heads of a query token.
+//
+// GB300 design (one CTA = one query token x one KV split, 512 threads):
+//  * Each KV tile is 128 selected rows.  Rows are gathered through the block
+//    table from the FP8 E4M3 cache, converted exactly to bf16 and stored ONCE
+//    in shared memory in the 128-byte-swizzled K-major layout.  That single
+//    copy is the A operand of  S^T = K Q^T  (M = 128 rows, N = 64 heads,
+//    K = 576) and, read MN-major, of  O^T = V^T P^T  (M = 4 x 128 latent
+//    dims, N = 64 heads, K = 128 rows).  Heads sit on N so every MMA has
+//    M = 128 and the full tensor-core datapath is used.
+//  * Accumulators live in tensor memory: S^T in 64 columns, O^T in 4 x 64.
+//  * The per-token dequantisation scale s_j is applied in fp32 where it is
+//    exact to do so: to the logits of row j, and folded into P before its
+//    bf16 rounding (P'_hj = p_hj s_j), so V stays raw FP8-valued bf16.
+//  * Online softmax in the log2 domain with lazy rescaling: the running max
+//    of a head is only raised (and O, l rescaled) when a tile's max exceeds
+//    it by more than 2^8; otherwise the stale max is kept, which is exact
+//    because O and l always share the same reference.
+//  * Warp roles: warp 0 allocates TMEM and one lane issues every MMA; warp 1
+//    resolves indices -> slots and scales 4 tiles ahead and prefetches the
+//    rows into L2; 6 converter warps gather + convert rows katom by katom
+//    (64-column slices) as soon as the previous tile's MMAs release them;
+//    8 softmax warps (2 per TMEM lane quadrant, 32 heads each) turn S into
+//    P and finally write O / l.  All hand-offs are mbarriers; every wait is
+//    bounded in time and reports DSA_DEV_TIMEOUT instead of hanging.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace dsa {
+namespace {
+
+using namespace sm100;
+
+constexpr int H = 64, DL = 512, DR = 64, DQK = DL + DR;
+constexpr int T = 128;                 // KV rows per tile
+constexpr int NKA = DQK / 64;          // 64-column slices ("katoms") per row: 9
+constexpr int KATOM_BYTES = T * 128;   // one slice of the KV tile: 128 rows x 128 B
+constexpr int QATOM_BYTES = H * 128;   // one slice of Q: 64 heads x 128 B
+constexpr int NST = 4;                 // index-ring stages
+constexpr int NTHREADS = 512;
+constexpr int NCONV = 6;               // converter warps
+constexpr int CONV_THREADS = NCONV * 32;
+constexpr int CHUNKS_PER_KATOM = T * 4;  // 16-byte FP8 chunks per slice
+constexpr int QD = 3;                  // converter prefetch depth (slices)
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+// TMEM columns
+constexpr uint32_t TM_S = 0;     // S^T: 64 columns
+constexpr uint32_t TM_O = 64;    // O^T chunk c at TM_O + 64 c
+constexpr uint32_t TM_COLS = 512;
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int OFF_KV = 0;
+constexpr int OFF_Q = OFF_KV + NKA * KATOM_BYTES;          // 147456
+constexpr int OFF_SLOT = OFF_Q + NKA * QATOM_BYTES;        // 221184
+constexpr int OFF_SCALE = OFF_SLOT + NST * T * 8;          // 225280
+constexpr int OFF_RED = OFF_SCALE + NST * T * 4;           // 227328
+constexpr int OFF_MUSE = OFF_RED + 4 * H * 4;              // 228352
+constexpr int OFF_ALPHA = OFF_MUSE + H * 4;                // 228608
+constexpr int OFF_FLAG = OFF_ALPHA + H * 4;                // 228864
+constexpr int OFF_BAR = OFF_FLAG + 64;                     // 228928
+// barrier indices
+constexpr int B_KV = 0;                 // [NKA] slice a of the current tile is in smem
+constexpr int B_SFULL = B_KV + NKA;     // S^T of the tile is in TMEM
+constexpr int B_PFULL = B_SFULL + 1;    // P of the tile is in smem (and O rescaled)
+constexpr int B_VFREE = B_PFULL + 1;    // [4] PV chunk c done: slices 2c, 2c+1 (c = 3: also slice 8) free
+constexpr int B_OFULL = B_VFREE + 4;    // all MMAs of the CTA done
+constexpr int B_IFULL = B_OFULL + 1;    // [NST] index stage filled
+constexpr int B_IFREE = B_IFULL + NST;  // [NST] index stage consumed
+constexpr int B_SYNCA = B_IFREE + NST;  // softmax-group sync points
+constexpr int B_SYNCB = B_SYNCA + 1;
+constexpr int B_FINAL = B_SYNCB + 1;
+constexpr int NBAR = B_FINAL + 1;
+constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+constexpr int SMEM_USED = OFF_TMEM + 16;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+constexpr int SOFTMAX_WARPS = 8;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint4 ldg_nc(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// two E4M3 values (low byte first) -> two bf16 (exact)
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two));
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// 16 E4M3 bytes -> 16 bf16 as two 16-byte chunks
+__device__ __forceinline__ void convert16(const uint4& v, uint4& lo, uint4& hi) {
+  lo.x = e4m3x2_to_bf16x2(v.x & 0xffffu);
+  lo.y = e4m3x2_to_bf16x2(v.x >> 16);
+  lo.z = e4m3x2_to_bf16x2(v.y & 0xffffu);
+  lo.w = e4m3x2_to_bf16x2(v.y >> 16);
+  hi.x = e4m3x2_to_bf16x2(v.z & 0xffffu);
+  hi.y = e4m3x2_to_bf16x2(v.z >> 16);
+  hi.z = e4m3x2_to_bf16x2(v.w & 0xffffu);
+  hi.w = e4m3x2_to_bf16x2(v.w >> 16);
+}
+
+// Offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte swizzled slice.
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// Per-warp transpose-reduction: v[32] per lane (32 heads) -> lane l returns
+// the reduction over the warp's 32 rows of head l.
+template <bool IS_MAX>
+__device__ __forceinline__ float warp_transpose_reduce(const float (&v)[32], int lane) {
+  float a16[16];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float send = up ? v[i] : v[i + 16];
+      const float keep = up ? v[i + 16] : v[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+      a16[i] = IS_MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  float a8[8];
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float send = up ? a16[i] : a16[i + 8];
+      const float keep = up ? a16[i + 8] : a16[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 8);
+      a8[i] = IS_MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  float a4[4];
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = up ? a8[i] : a8[i + 4];
+      const float keep = up ? a8[i + 4] : a8[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 4);
+      a4[i] = IS_MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  float a2[2];
+  {
+    const bool up = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = up ? a4[i] : a4[i + 2];
+      const float keep = up ? a4[i + 2] : a4[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 2);
+      a2[i] = IS_MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  const bool up = lane & 1;
+  const float send = up ? a2[0] : a2[1];
+  const float keep = up ? a2[1] : a2[0];
+  const float got = __shfl_xor_sync(0xffffffffu, send, 1);
+  return IS_MAX ? fmaxf(keep, got) : keep + got;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* kv_s = smem + OFF_KV;
+  unsigned char* q_s = smem + OFF_Q;
+  int64_t* slot_s = reinterpret_cast<int64_t*>(smem + OFF_SLOT);
+  float* scale_s = reinterpret_cast<float*>(smem + OFF_SCALE);
+  float* red_s = reinterpret_cast<float*>(smem + OFF_RED);
+  float* muse_s = reinterpret_cast<float*>(smem + OFF_MUSE);
+  float* alpha_s = reinterpret_cast<float*>(smem + OFF_ALPHA);
+  int* flag_s = reinterpret_cast<int*>(smem + OFF_FLAG);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+  auto bar = [&](int b) { return smem_u32(bars + b); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = blockIdx.x;        // query token
+  const int split = blockIdx.y;
+  const int S = gridDim.y;
+  const int ntiles = (a.k + T - 1) / T;
+  const int t_begin = (int)((int64_t)ntiles * split / S);
+  const int t_end = (int)((int64_t)ntiles * (split + 1) / S);
+  const int ntl = t_end - t_begin;
+
+  if (ntl == 0) {  // an empty split: O = 0, lse = -inf
+    for (int e = tid; e < H * DL; e += NTHREADS) {
+      if (S == 1)
+        static_cast<__nv_bfloat16*>(a.out)[(int64_t)i * H * DL + e] = __float2bfloat16_rn(0.f);
+      else
+        a.o_part[((int64_t)split * a.num_q + i) * H * DL + e] = 0.f;
+    }
+    for (int h = tid; h < H; h += NTHREADS) {
+      if (S == 1) {
+        if (a.lse) a.lse[(int64_t)i * H + h] = -INFINITY;
+      } else {
+        a.lse_part[((int64_t)split * a.num_q + i) * H + h] = -INFINITY;
+      }
+    }
+    return;
+  }
+
+  // ---------------- setup ----------------
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), TM_COLS);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int b = 0; b < NKA; ++b) mbar_init(bar(B_KV + b), NCONV);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_PFULL), SOFTMAX_WARPS);
+    for (int c = 0; c < 4; ++c) mbar_init(bar(B_VFREE + c), 1);
+    mbar_init(bar(B_OFULL), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar(B_IFULL + s), 32);
+      mbar_init(bar(B_IFREE + s), NCONV + SOFTMAX_WARPS);
+    }
+    mbar_init(bar(B_SYNCA), SOFTMAX_WARPS);
+    mbar_init(bar(B_SYNCB), SOFTMAX_WARPS);
+    mbar_init(bar(B_FINAL), 1);
+    fence_mbarrier_init();
+  }
+  if (tid < H) {
+    muse_s[tid] = -INFINITY;
+    alpha_s[tid] = 1.f;
+  }
+  // Q of this token -> swizzled K-major slices
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK);
+    constexpr int CH = DQK / 8;
+    for (int e = tid; e < H * CH; e += NTHREADS) {
+      const int h = e / CH, cc = e % CH;
+      *reinterpret_cast<uint4*>(q_s + (cc >> 3) * QATOM_BYTES + sw128(h, cc & 7)) = src[e];
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const int r = a.q_req[i];
+  const bool req_ok = (r >= 0 && r < a.num_req);
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      if (!req_ok) report(a.dev_status, DSA_DEV_BAD_PAGE);
+      constexpr uint32_t ID_QK = idesc_bf16_f32(128, 64, 0, 0);
+      constexpr uint32_t ID_PV = idesc_bf16_f32(128, 64, 1, 1);
+      const uint32_t kv_base = smem_u32(kv_s), q_base = smem_u32(q_s);
+      const uint32_t p_base = kv_base + 8 * KATOM_BYTES;
+      for (int lt = 0; lt < ntl && ok; ++lt) {
+        const uint32_t par = lt & 1;
+        for (int ka = 0; ka < NKA && ok; ++ka) {
+          if (!mbar_wait(bar(B_KV + ka), par)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc_sw128(kv_base + ka * KATOM_BYTES + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(q_base + ka * QATOM_BYTES + kk * 32, 16, 1024);
+            mma_bf16_ss(tmem + TM_S, ad, bd, ID_QK, (ka | kk) != 0);
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(B_SFULL));
+        if (!mbar_wait(bar(B_PFULL), par)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = smem_desc_sw128(kv_base + 2 * c * KATOM_BYTES + kk * 2048, KATOM_BYTES, 1024);
+            const uint64_t bd = smem_desc_sw128(p_base + kk * 2048, KATOM_BYTES, 1024);
+            mma_bf16_ss(tmem + TM_O + 64 * c, ad, bd, ID_PV, (lt > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(B_VFREE + c));
+        }
+      }
+      mma_commit(bar(B_OFULL));
+      mma_commit(bar(B_FINAL));
+      if (!ok) report(a.dev_status, DSA_DEV_TIMEOUT);
+      // all issued MMAs must be finished before TMEM is released
+      if (!mbar_wait(bar(B_FINAL), 0)) report(a.dev_status, DSA_DEV_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- index warp: positions -> slots, scales, L2 prefetch ----------------
+    const int32_t* row_idx = a.idx + (int64_t)i * a.k;
+    for (int lt = 0; lt < ntl; ++lt) {
+      const int st = lt % NST;
+      if (lt >= NST && !mbar_wait(bar(B_IFREE + st), ((lt / NST) - 1) & 1)) {
+        report(a.dev_status, DSA_DEV_TIMEOUT);
+        break;
+      }
+      const int tile = t_begin + lt;
+#pragma unroll
+      for (int jj = 0; jj < T / 32; ++jj) {
+        const int j = lane + 32 * jj;
+        const int e = tile * T + j;
+        int64_t slot = -1;
+        float sc = 0.f;
+        if (e < a.k && req_ok) {
+          const int32_t pos = row_idx[e];
+          if (pos < -1) {
+            report(a.dev_status, DSA_DEV_BAD_INDEX);
+          } else if (pos >= 0) {
+            const int32_t pg = pos / a.page_size;
+            if (pg >= a.bt_stride) {
+              report(a.dev_status, DSA_DEV_BAD_INDEX);
+            } else {
+              const int32_t page = a.block_table[(int64_t)r * a.bt_stride + pg];
+              if (page < 0 || page >= a.num_pages) {
+                report(a.dev_status, DSA_DEV_BAD_PAGE);
+              } else {
+                slot = (int64_t)page * a.page_size + pos % a.page_size;
+                sc = a.kv_scale[slot];
+                prefetch_l2(a.kv + slot * DQK, DQK);
+              }
+            }
+          }
+        }
+        slot_s[st * T + j] = slot;
+        scale_s[st * T + j] = sc;
+      }
+      mbar_arrive(bar(B_IFULL + st));
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------- softmax warps ----------------
+    const int q4 = warp & 3;            // TMEM lane quadrant
+    const int half = (warp - 4) >> 2;   // heads [32 half, 32 half + 32)
+    const int j = 32 * q4 + lane;       // KV row of the tile = TMEM lane
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
+    const float qk_scale = a.softmax_scale * LOG2E;
+    unsigned char* p_row = kv_s + 8 * KATOM_BYTES;
+    float l_part[32];
+#pragma unroll
+    for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
+    uint32_t sync_phase = 0;
+    for (int lt = 0; lt < ntl && ok; ++lt) {
+      const int st = lt % NST;
+      if (!mbar_wait(bar(B_IFULL + st), (lt / NST) & 1) || !mbar_wait(bar(B_SFULL), lt & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const bool valid = slot_s[st * T + j] >= 0;
+      const float sc = scale_s[st * T + j];
+      const float cj = sc * qk_scale;
+      // logits of row j in the log2 domain (invalid rows: -inf)
+      auto load_z = [&](float (&z)[32]) {
+        float v[16], w[16];
+        tmem_ld16(t_lane + TM_S + half * 32, v);
+        tmem_ld16(t_lane + TM_S + half * 32 + 16, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          z[h] = valid ? v[h] * cj : -INFINITY;
+          z[h + 16] = valid ? w[h] * cj : -INFINITY;
+        }
+      };
+      {
+        float z[32];
+        load_z(z);
+        red_s[q4 * H + half * 32 + lane] = warp_transpose_reduce<true>(z, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SYNCA));
+      if (!mbar_wait(bar(B_SYNCA), sync_phase & 1)) {
+        ok = false;
+        break;
+      }
+      if (q4 == 0) {  // warps 4 and 8 own 32 heads each
+        const int hh = half * 32 + lane;
+        const float mt = fmaxf(fmaxf(red_s[hh], red_s[H + hh]), fmaxf(red_s[2 * H + hh], red_s[3 * H + hh]));
+        const float mo = muse_s[hh];
+        float alpha = 1.f;
+        if (mt > mo + RESCALE_LOG2) {
+          alpha = (mo == -INFINITY) ? 0.f : ex2(mo - mt);
+          muse_s[hh] = mt;
+        }
+        alpha_s[hh] = alpha;
+        const unsigned need = __ballot_sync(0xffffffffu, lt > 0 && alpha != 1.f);
+        if (lane == 0) flag_s[half] = need != 0u;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SYNCB));
+      if (!mbar_wait(bar(B_SYNCB), sync_phase & 1)) {
+        ok = false;
+        break;
+      }
+      ++sync_phase;
+      const bool rescale = flag_s[half] != 0;
+      if (rescale) {
+        const float* al = alpha_s + half * 32;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) l_part[h] *= al[h];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            float o[16];
+            const uint32_t addr = t_lane + TM_O + 64 * c + half * 32 + 16 * g;
+            tmem_ld16(addr, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 16; ++h) o[h] *= al[16 * g + h];
+            tmem_st16(addr, o);
+          }
+        }
+        tmem_wait_st();
+      }
+      // probabilities, folded with the row's dequantisation scale, as bf16 P
+      // (S is still in TMEM: reload it rather than keep it live across the rescale)
+      float z[32];
+      load_z(z);
+      uint32_t pk[16];
+#pragma unroll
+      for (int h2 = 0; h2 < 16; ++h2) {
+        const float m0 = muse_s[half * 32 + 2 * h2], m1 = muse_s[half * 32 + 2 * h2 + 1];
+        const float p0 = valid ? ex2(z[2 * h2] - m0) : 0.f;
+        const float p1 = valid ? ex2(z[2 * h2 + 1] - m1) : 0.f;
+        l_part[2 * h2] += p0;
+        l_part[2 * h2 + 1] += p1;
+        const __nv_bfloat162 b = __floats2bfloat162_rn(p0 * sc, p1 * sc);
+        pk[h2] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        *reinterpret_cast<uint4*>(p_row + sw128(j, half * 4 + cc)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_PFULL));
+        mbar_arrive(bar(B_IFREE + st));
+      }
+    }
+    // ---------------- epilogue: normalise and write ----------------
+    if (ok && !mbar_wait(bar(B_OFULL), 0)) ok = false;
+    if (ok) {
+      tc_fence_after_sync();
+      const float ws = warp_transpose_reduce<false>(l_part, lane);
+      red_s[q4 * H + half * 32 + lane] = ws;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SYNCA));
+      ok = mbar_wait(bar(B_SYNCA), sync_phase & 1);
+    }
+    if (ok) {
+      if (q4 == 0) {
+        const int hh = half * 32 + lane;
+        const float l = red_s[hh] + red_s[H + hh] + red_s[2 * H + hh] + red_s[3 * H + hh];
+        const float m = muse_s[hh];
+        alpha_s[hh] = l > 0.f ? 1.f / l : 0.f;
+        const float lse = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+        if (S == 1) {
+          if (a.lse) a.lse[(int64_t)i * H + hh] = lse;
+        } else {
+          a.lse_part[((int64_t)split * a.num_q + i) * H + hh] = lse;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SYNCB));
+      ok = mbar_wait(bar(B_SYNCB), sync_phase & 1);
+    }
+    if (ok) {
+      const float* inv = alpha_s + half * 32;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int d = 128 * c + 32 * q4 + lane;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          float o[16];
+          tmem_ld16(t_lane + TM_O + 64 * c + half * 32 + 16 * g, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            const int hh = half * 32 + 16 * g + h;
+            const float val = o[h] * inv[16 * g + h];
+            const int64_t off = ((int64_t)i * H + hh) * DL + d;
+            if (S == 1)
+              static_cast<__nv_bfloat16*>(a.out)[off] = __float2bfloat16_rn(val);
+            else
+              a.o_part[(int64_t)split * a.num_q * H * DL + off] = val;
+          }
+        }
+      }
+    } else {
+      report(a.dev_status, DSA_DEV_TIMEOUT);
+    }
+  } else {
+    // ---------------- converter warps: gather FP8 rows, convert, store swizzled bf16 ----------------
+    const int ctid = (warp < 4 ? (warp - 2) : (warp - 12 + 2)) * 32 + lane;  // 0..191
+    const int nitems = ntl * NKA;
+    uint4 buf[QD][3];
+    int loaded_lt = -1;
+
+    auto load_item = [&](int m, uint4 (&b)[3]) {
+      const int lt = m / NKA, ka = m % NKA, st = lt % NST;
+      if (lt != loaded_lt) {
+        if (!mbar_wait(bar(B_IFULL + st), (lt / NST) & 1)) ok = false;
+        loaded_lt = lt;
+      }
+#pragma unroll
+      for (int rr = 0; rr < 3; ++rr) {
+        const int e = ctid + CONV_THREADS * rr;
+        b[rr] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < CHUNKS_PER_KATOM && ok) {
+          const int row = e >> 2, c16 = e & 3;
+          const int64_t slot = slot_s[st * T + row];
+          if (slot >= 0) b[rr] = ldg_nc(a.kv + slot * DQK + ka * 64 + c16 * 16);
+        }
+      }
+      if (ka == NKA - 1) {  // last slice of the tile: this warp is done with the index stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_IFREE + st));
+      }
+    };
+
+#pragma unroll
+    for (int u = 0; u < QD; ++u)
+      if (u < nitems) load_item(u, buf[u]);
+    for (int n = 0; n < nitems && ok; n += QD) {
+#pragma unroll
+      for (int u = 0; u < QD; ++u) {
+        const int m = n + u;
+        if (m >= nitems || !ok) break;
+        const int lt = m / NKA, ka = m % NKA;
+        if (lt > 0) {
+          const int c = ka < 8 ? (ka >> 1) : 3;
+          if (!mbar_wait(bar(B_VFREE + c), (lt - 1) & 1)) {
+            ok = false;
+            break;
+          }
+        }
+        unsigned char* dst = kv_s + ka * KATOM_BYTES;
+#pragma unroll
+        for (int rr = 0; rr < 3; ++rr) {
+          const int e = ctid + CONV_THREADS * rr;
+          if (e < CHUNKS_PER_KATOM) {
+            const int row = e >> 2, c16 = e & 3;
+            uint4 lo, hi;
+            convert16(buf[u][rr], lo, hi);
+            *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16)) = lo;
+            *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + 1)) = hi;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_KV + ka));
+        if (m + QD < nitems) load_item(m + QD, buf[u]);
+      }
+    }
+    if (!ok) report(a.dev_status, DSA_DEV_TIMEOUT);
+  }
+
+  // ---------------- teardown ----------------
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+}
+
+}  // namespace
+
+bool mla_tc_supported(const MlaArgs& a) { return a.heads == H && a.d_latent == DL && a.d_rope == DR; }
+
+cudaError_t launch_mla_tc(const MlaArgs& a, cudaStream_t stream) {
+  if (a.num_q == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_q, a.num_splits);
+  mla_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -56,17 +56,23 @@ def test_tile_count_worked_example(lib):
 
 
 def test_split_rule(lib):
-    """Splits only when query tokens alone leave SMs idle; never more splits
-    than KV tiles."""
+    """Splits only when query tokens alone leave SMs idle and splitting
+    shortens the launch; never more splits than KV tiles."""
     tile = dsa.kv_tile_size(64, 512, 64)
-    assert tile > 0 and dsa.kv_tile_size(32, 512, 64) == -1
+    assert tile == 128 and dsa.kv_tile_size(16, 64, 16) == 32 and dsa.kv_tile_size(32, 512, 64) == -1
+    ntiles = dsa.kv_tile_count(2048, tile)
     assert dsa.pick_num_splits(32768, 64, 512, 64, 2048, num_sms=152) == 1
     assert dsa.pick_num_splits(1024, 64, 512, 64, 2048, num_sms=152) == 1
-    s_dec = dsa.pick_num_splits(128, 64, 512, 64, 2048, num_sms=152)
-    assert 1 < s_dec <= dsa.kv_tile_count(2048, tile)
+    # 128 decode tokens on 152 SMs: one wave without splitting; splitting
+    # would only add waves, partial writes and a combine
+    assert dsa.pick_num_splits(128, 64, 512, 64, 2048, num_sms=152) == 1
+    # 16 tokens of 1M context: split until the SMs are busy
     s_1m = dsa.pick_num_splits(16, 64, 512, 64, 2048, num_sms=152)
-    assert s_1m >= s_dec
-    assert dsa.pick_num_splits(2, 16, 64, 16, 64, num_sms=152) <= dsa.kv_tile_count(64, dsa.kv_tile_size(16, 64, 16))
+    assert 4 <= s_1m <= ntiles and 16 * s_1m <= 152
+    assert dsa.pick_num_splits(1, 64, 512, 64, 100, num_sms=152) == 1  # a single tile cannot split
+    for nq in (1, 2, 5, 16, 40, 100):
+        s = dsa.pick_num_splits(nq, 64, 512, 64, 2048, num_sms=152)
+        assert 1 <= s <= ntiles
 
 
 # ---- argument validation: every case returns before any CUDA call ----

@@ -251,3 +251,34 @@ def test_permuted_indices_give_same_output():
     o2, l2 = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx2, **kw)
     torch.cuda.synchronize()
     assert (o1.float() - o2.float()).abs().max().item() <= 4e-3
+
+
+def test_tensor_core_kernel_matches_cuda_core_kernel(monkeypatch):
+    """The tcgen05 kernel and the fp32 CUDA-core kernel agree on the same
+    selection (both are also checked against the oracle above)."""
+    w = SMALL_H64
+    inp = inputs(w)
+    idx = dsa.topk_select(inp.scores, inp.q_pos, w.k)
+    kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+    o_tc, l_tc = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, **kw)
+    torch.cuda.synchronize()
+    monkeypatch.setenv("DSA_FORCE_SIMT", "1")
+    o_s, l_s = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, **kw)
+    torch.cuda.synchronize()
+    assert (o_tc.float() - o_s.float()).abs().max().item() <= 4e-3
+    assert (l_tc - l_s).abs().max().item() <= 1e-3
+
+
+def test_large_logit_range_triggers_rescale():
+    """Queries scaled up so that later tiles raise the running max by far more
+    than the lazy-rescale threshold: the result must still match the oracle."""
+    w = wl.Workload("rescale_h64", 2, 2, 64, 512, 64, 1500, 0, 64, 1024, seed=31)
+    inp = wl.make_inputs(w, device="cuda")
+    # large queries: logits ~ N(0, 36), so later tiles beat the first tile's
+    # maximum by more than 2^8 and the accumulators must be rescaled
+    inp.q.mul_(6.0)
+    out, lse, idx = run(inp)
+    rows = np.arange(w.num_q)
+    ref_idx, ref_out, ref_lse = oracle_rows(inp, rows)
+    assert np.array_equal(host(idx), ref_idx)
+    assert_close(host(out.float()), host(lse), ref_out, ref_lse, w.name)
