@@ -18,6 +18,19 @@ dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR
 
 }  // namespace
 
+namespace dsa {
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+}  // namespace dsa
+
 extern "C" {
 
 const char* dsa_status_string(int32_t status) {
@@ -47,12 +60,7 @@ int32_t dsa_pick_num_splits(int32_t num_q, int32_t num_heads, int32_t d_latent, 
                             int32_t num_sms) {
   const int32_t tile = dsa_kv_tile_size(num_heads, d_latent, d_rope);
   if (tile <= 0 || num_q <= 0 || k <= 0) return 1;
-  if (num_sms <= 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      num_sms = 148;
-  }
+  if (num_sms <= 0) num_sms = dsa::device_sm_count();
   // query tokens alone fill the GPU: no split (no partials, no combine)
   if (num_q >= num_sms) return 1;
   // One CTA per SM (shared memory bound); a launch takes ceil(CTAs / SMs)
@@ -83,8 +91,8 @@ dsa_status dsa_topk_select(const float* scores, int64_t ld_scores, const int32_t
   if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
   if (workspace_bytes < dsa_topk_workspace_size(num_q, ld_scores, k)) return DSA_ERR_WORKSPACE_TOO_SMALL;
   (void)workspace;
-  return from_cuda(dsa::launch_topk_radix(scores, ld_scores, q_pos, num_q, k, idx, dev_status,
-                                          static_cast<cudaStream_t>(stream)));
+  return from_cuda(dsa::launch_topk(scores, ld_scores, q_pos, num_q, k, idx, dev_status,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_scale, int64_t num_pages,

@@ -9,8 +9,13 @@
 namespace dsa {
 
 // Kernel launchers (each returns the launch's cudaError_t).
-cudaError_t launch_topk_radix(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
-                              int32_t* idx, int32_t* dev_status, cudaStream_t stream);
+cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
+                        int32_t* idx, int32_t* dev_status, cudaStream_t stream);
+// CTAs per top-k row (a thread-block cluster) for this launch.
+int topk_cluster_size(int32_t num_q, int64_t ld, int num_sms);
+
+// SM count of the current device (cached per device).
+int device_sm_count();
 
 struct MlaArgs {
   const void* q;

@@ -1,4 +1,4 @@
-// Causal top-k selection over fp32 indexer scores (radix select).
+// Causal top-k selection over fp32 indexer scores.
 //
 // "Accelerating GLM-5.3-Flash on H200", section 3 "Larger KV tiles for DSA
 // Partial": the indexer's scores pick the KV positions the Partial step
@@ -6,21 +6,35 @@
 // are ranked by (score descending, position ascending), -0.0 == +0.0, and
 // the chosen ones are written in ascending position order, -1 padded.
 //
-// Method: every fp32 score maps to an order-preserving 32-bit key.  A radix
-// select over the key's digits (11, 11, 10 bits) finds the exact key T of the
-// k-th largest visible score and how many of the entries equal to T must be
-// taken.  One more ordered pass then writes every position whose key beats T
-// and the lowest-positioned entries equal to T, using block-wide prefix sums
-// so that output order is ascending position order.
+// Every fp32 score maps to an order-preserving 32-bit key.  A row is handled
+// by a thread-block cluster of C CTAs, each owning a contiguous slice of the
+// visible positions:
+//   1. each CTA histograms the top 12 key bits of a 1/16 sample of its slice;
+//      the histograms are summed over the cluster (distributed shared memory)
+//      and give a lower threshold T_lo that, with a wide safety margin, lies
+//      below the k-th largest key;
+//   2. one streaming pass collects every key >= T_lo with its position, in
+//      position order (warp ballots + a scan of warp counts);
+//   3. CTA 0 gathers the candidates of the cluster, finds the exact key T of
+//      the k-th largest entry by radix select over the candidates, and writes
+//      the keys above T plus the lowest-positioned entries equal to T.
+// If the sample misleads (fewer than k candidates, or more than fit), CTA 0
+// falls back to an exact multi-pass radix select over the whole row in
+// global memory, so the result never depends on the score distribution.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include "internal.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace dsa {
 namespace {
 
-constexpr int kTopkThreads = 1024;
-constexpr int kBins = 2048;
+constexpr int NT = 1024;          // threads per CTA
+constexpr int HBINS = 4096;       // histogram bins (12 key bits)
+constexpr int MCAP = 8192;        // candidates CTA 0 can hold for the final selection
+constexpr int SAMPLE_SHIFT = 7;   // sample the first 8 of every 128 positions (1/16)
 
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -28,15 +42,14 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix sum of one value per thread over the whole block; *total
-// receives the block sum.  `warp_buf` holds NT/32 words of shared memory.
-template <int NT>
+// Exclusive prefix sum of one value per thread over the block; *total gets
+// the block sum.  `warp_buf` holds 32 words of shared memory.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* total, uint32_t* warp_buf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) warp_buf[warp] = x;
@@ -45,7 +58,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
     uint32_t w = lane < NT / 32 ? warp_buf[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
     if (lane < NT / 32) warp_buf[lane] = w;
@@ -57,125 +70,297 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
   return before + x - v;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_radix_kernel(const float* __restrict__ scores, int64_t ld,
-                                                                  const int32_t* __restrict__ q_pos, int32_t k,
-                                                                  int32_t* __restrict__ idx, int32_t* status) {
-  constexpr int NT = kTopkThreads;
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t warp_buf[NT / 32];
-  __shared__ uint32_t sel_bin, sel_above, sel_count;
-
-  const int64_t row = blockIdx.x;
-  const int tid = threadIdx.x;
-  int32_t* out = idx + row * (int64_t)k;
-  const int64_t p = q_pos[row];
-  if (p < 0 || p >= ld) {
-    if (tid == 0) report(status, DSA_DEV_BAD_QPOS);
-    for (int j = tid; j < k; j += NT) out[j] = -1;
-    return;
+// Among the keys in bins [0, nbins) of `hist` counted from the top, find the
+// bin holding the krem-th largest key.  Every thread returns the same
+// (bin, count above the bin, count in the bin).
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32_t krem, uint32_t* warp_buf,
+                                         uint32_t* sel, uint32_t& bin, uint32_t& above, uint32_t& count) {
+  const int per = nbins / NT;  // 2 or 4 bins per thread, highest bins to thread 0
+  uint32_t c[4] = {0u, 0u, 0u, 0u};
+  uint32_t sum = 0;
+  for (int t = 0; t < per; ++t) {
+    c[t] = hist[nbins - 1 - (threadIdx.x * per + t)];
+    sum += c[t];
   }
-  const int64_t vis = p + 1;
-  if (vis <= k) {  // everything visible is selected
-    for (int j = tid; j < k; j += NT) out[j] = j < vis ? j : -1;
-    return;
+  uint32_t total;
+  uint32_t acc = block_exclusive_scan(sum, &total, warp_buf);
+  for (int t = 0; t < per; ++t) {
+    if (acc < krem && krem <= acc + c[t]) {
+      sel[0] = nbins - 1 - (threadIdx.x * per + t);
+      sel[1] = acc;
+      sel[2] = c[t];
+    }
+    acc += c[t];
   }
-  const float* s = scores + row * ld;
-  const bool vec = ((reinterpret_cast<uintptr_t>(s) & 15u) == 0);
-  const int64_t vis4 = vec ? (vis & ~int64_t(3)) : 0;
+  __syncthreads();
+  bin = sel[0], above = sel[1], count = sel[2];
+  __syncthreads();
+}
 
-  // ---- radix select: find the key prefix of the k-th largest score ----
-  uint32_t prefix = 0, mask = 0;
-  uint32_t krem = (uint32_t)k;
+// Exact selection over n keys with positions (keys/pos in any memory, in
+// ascending position order): writes the k chosen positions ascending.
+template <bool GLOBAL_ROW>
+__device__ void select_exact(const float* row_scores, const uint32_t* keys, const int32_t* pos, int64_t n, uint32_t k,
+                             int32_t* out, uint32_t* hist, uint32_t* warp_buf, uint32_t* sel) {
+  auto key_at = [&](int64_t e) -> uint32_t { return GLOBAL_ROW ? score_key(row_scores[e]) : keys[e]; };
+  auto pos_at = [&](int64_t e) -> int32_t { return GLOBAL_ROW ? (int32_t)e : pos[e]; };
+  uint32_t prefix = 0, mask = 0, krem = k;
   const int shifts[3] = {21, 10, 0};
-  const uint32_t digit_mask[3] = {0x7ffu, 0x7ffu, 0x3ffu};
+  const uint32_t dmask[3] = {0x7ffu, 0x7ffu, 0x3ffu};
   for (int pass = 0; pass < 3; ++pass) {
     const int sh = shifts[pass];
-    const uint32_t dm = digit_mask[pass];
-    for (int b = tid; b < kBins; b += NT) hist[b] = 0;
+    const uint32_t dm = dmask[pass];
+    for (int b = threadIdx.x; b < 2048; b += NT) hist[b] = 0;
     __syncthreads();
-    for (int64_t j = int64_t(tid) * 4; j < vis4; j += int64_t(NT) * 4) {
-      const float4 v = *reinterpret_cast<const float4*>(s + j);
-      const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint32_t key = score_key(e[t]);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
-      }
-    }
-    for (int64_t j = vis4 + tid; j < vis; j += NT) {
-      const uint32_t key = score_key(s[j]);
+    for (int64_t e = threadIdx.x; e < n; e += NT) {
+      const uint32_t key = key_at(e);
       if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
     }
     __syncthreads();
-    // bins in descending order: thread t owns bins kBins-1-2t and kBins-2-2t
-    const int b0 = kBins - 1 - 2 * tid, b1 = b0 - 1;
-    const uint32_t c0 = hist[b0], c1 = hist[b1];
-    uint32_t total;
-    uint32_t above = block_exclusive_scan<NT>(c0 + c1, &total, warp_buf);
-    if (above < krem && krem <= above + c0) {
-      sel_bin = b0, sel_above = above, sel_count = c0;
-    }
-    above += c0;
-    if (above < krem && krem <= above + c1) {
-      sel_bin = b1, sel_above = above, sel_count = c1;
-    }
-    __syncthreads();
-    prefix |= sel_bin << sh;
+    uint32_t bin, above, count;
+    find_bin(hist, 2048, krem, warp_buf, sel, bin, above, count);
+    prefix |= bin << sh;
     mask |= dm << sh;
-    krem -= sel_above;
-    const bool whole_bin = (sel_count == krem);
-    __syncthreads();  // everyone has read sel_* before the next pass rewrites them
-    if (whole_bin) break;  // every entry of the bin is taken: no need to refine further
+    krem -= above;
+    if (count == krem) break;  // the whole bin is taken
   }
-
-  // ---- ordered compaction: keys above the prefix, then the first krem ties ----
+  // ordered output: keys above the prefix, then the first krem equal ones
   uint32_t ties_before = 0, written = 0;
-  for (int64_t base = 0; base < vis && written < (uint32_t)k; base += int64_t(NT) * 4) {
-    const int64_t j0 = base + int64_t(tid) * 4;
-    float e[4];
-    if (vec && j0 + 3 < vis) {
-      const float4 v = *reinterpret_cast<const float4*>(s + j0);
-      e[0] = v.x, e[1] = v.y, e[2] = v.z, e[3] = v.w;
-    } else {
-#pragma unroll
-      for (int t = 0; t < 4; ++t) e[t] = (j0 + t < vis) ? s[j0 + t] : 0.f;
-    }
+  constexpr int PER = 4;
+  for (int64_t base = 0; base < n && written < k; base += (int64_t)NT * PER) {
+    const int64_t e0 = base + (int64_t)threadIdx.x * PER;
     uint32_t gt = 0, eq = 0;
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      if (j0 + t < vis) {
-        const uint32_t mk = score_key(e[t]) & mask;
-        gt |= (mk > prefix) << t;
-        eq |= (mk == prefix) << t;
+    for (int t = 0; t < PER; ++t) {
+      if (e0 + t < n) {
+        const uint32_t mk = key_at(e0 + t) & mask;
+        gt |= (uint32_t)(mk > prefix) << t;
+        eq |= (uint32_t)(mk == prefix) << t;
       }
     }
     uint32_t eq_total;
-    uint32_t rank = ties_before + block_exclusive_scan<NT>(__popc(eq), &eq_total, warp_buf);
+    uint32_t rank = ties_before + block_exclusive_scan(__popc(eq), &eq_total, warp_buf);
     uint32_t take = gt;
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    for (int t = 0; t < PER; ++t) {
       if ((eq >> t) & 1u) {
         if (rank < krem) take |= 1u << t;
         ++rank;
       }
     }
     uint32_t take_total;
-    uint32_t o = written + block_exclusive_scan<NT>(__popc(take), &take_total, warp_buf);
+    uint32_t o = written + block_exclusive_scan(__popc(take), &take_total, warp_buf);
 #pragma unroll
-    for (int t = 0; t < 4; ++t)
-      if ((take >> t) & 1u) out[o++] = (int32_t)(j0 + t);
+    for (int t = 0; t < PER; ++t)
+      if (((take >> t) & 1u) && o < k) out[o++] = pos_at(e0 + t);
     ties_before += eq_total;
     written += take_total;
   }
 }
 
+template <int C>
+struct TopkSmem {
+  static constexpr int LCAP = C == 1 ? MCAP : 4096;  // candidates one CTA collects
+  static constexpr size_t bytes = sizeof(uint32_t) * HBINS + (sizeof(uint32_t) + sizeof(int32_t)) * LCAP +
+                                  (C > 1 ? (sizeof(uint32_t) + sizeof(int32_t)) * MCAP : 0);
+};
+
+template <int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 1)
+    topk_cluster_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ q_pos, int32_t k,
+                        int32_t* __restrict__ idx, int32_t* status) {
+  constexpr int LCAP = TopkSmem<C>::LCAP;
+  extern __shared__ __align__(16) uint32_t smem[];
+  uint32_t* hist = smem;
+  uint32_t* ckey = hist + HBINS;
+  int32_t* cpos = reinterpret_cast<int32_t*>(ckey + LCAP);
+  uint32_t* mkey = C > 1 ? reinterpret_cast<uint32_t*>(cpos + LCAP) : ckey;
+  int32_t* mpos = C > 1 ? reinterpret_cast<int32_t*>(mkey + MCAP) : cpos;
+  __shared__ uint32_t warp_buf[32];
+  __shared__ uint32_t sel[4];
+  // vars: [0] T_lo (CTA 0), [1] candidate count, [2] overflow, [3] sampled count
+  __shared__ uint32_t vars[4];
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x / C;
+  int32_t* out = idx + row * (int64_t)k;
+  const int64_t p = q_pos[row];
+  // row-uniform early exits (the same for every CTA of the cluster)
+  if (p < 0 || p >= ld) {
+    if (rank == 0) {
+      if (tid == 0) report(status, DSA_DEV_BAD_QPOS);
+      for (int j = tid; j < k; j += NT) out[j] = -1;
+    }
+    return;
+  }
+  const int64_t vis = p + 1;
+  if (vis <= k) {
+    if (rank == 0)
+      for (int j = tid; j < k; j += NT) out[j] = j < vis ? j : -1;
+    return;
+  }
+  const float* s = scores + row * ld;
+  const bool vec = ((reinterpret_cast<uintptr_t>(s) & 15u) == 0);
+  // this CTA's slice [lo, hi), a multiple of 128 positions long
+  const int64_t per = ((vis + C - 1) / C + 127) & ~int64_t(127);
+  const int64_t lo = (int64_t)rank * per;
+  const int64_t hi = lo + per < vis ? lo + per : vis;
+
+  // ---- 1. sampled histogram of the top 12 key bits ----
+  for (int b = tid; b < HBINS; b += NT) hist[b] = 0;
+  if (tid == 0) vars[1] = vars[2] = 0;
+  __syncthreads();
+  uint32_t nsampled = 0;
+  for (int64_t blk = lo + (int64_t)tid * 128; blk < hi; blk += (int64_t)NT * 128) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      if (blk + t < hi) {
+        atomicAdd(&hist[score_key(__ldg(s + blk + t)) >> 20], 1u);
+        ++nsampled;
+      }
+    }
+  }
+  {
+    uint32_t tot;
+    block_exclusive_scan(nsampled, &tot, warp_buf);
+    if (tid == 0) vars[3] = tot;
+  }
+  cluster.sync();
+  if (rank == 0) {
+    // sum the cluster's histograms into this CTA's, then place T_lo so that
+    // the sample above it exceeds its expected share of the top k by 25% + 16
+    for (int r = 1; r < C; ++r) {
+      const uint32_t* rh = cluster.map_shared_rank(hist, r);
+      for (int b = tid; b < HBINS; b += NT) hist[b] += rh[b];
+    }
+    uint32_t ns = vars[3];
+    for (int r = 1; r < C; ++r) ns += *cluster.map_shared_rank(&vars[3], r);
+    __syncthreads();
+    uint32_t t_lo = 0;
+    if (vis > MCAP / 2 && ns > 0) {
+      const double expect = (double)k * (double)ns / (double)vis;
+      uint32_t need = (uint32_t)(expect * 1.25) + 16u;
+      if (need > ns) need = ns;
+      uint32_t bin, above, count;
+      find_bin(hist, HBINS, need > 0 ? need : 1u, warp_buf, sel, bin, above, count);
+      t_lo = bin << 20;
+    }
+    if (tid == 0) vars[0] = t_lo;
+  }
+  cluster.sync();
+  const uint32_t t_lo = *cluster.map_shared_rank(&vars[0], 0);
+
+  // ---- 2. ordered collection of the candidates (key >= T_lo) ----
+  constexpr int PER = 16;  // contiguous positions per thread per step
+  uint32_t written = 0;
+  bool overflow = false;
+  for (int64_t base = lo; base < hi; base += (int64_t)NT * PER) {
+    const int64_t e0 = base + (int64_t)tid * PER;
+    float v[PER];
+    if (vec && e0 + PER <= hi) {
+#pragma unroll
+      for (int t = 0; t < PER / 4; ++t) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(s + e0) + t);
+        v[4 * t] = f.x, v[4 * t + 1] = f.y, v[4 * t + 2] = f.z, v[4 * t + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < PER; ++t) v[t] = (e0 + t < hi) ? __ldg(s + e0 + t) : -INFINITY;
+    }
+    uint32_t flags = 0;
+#pragma unroll
+    for (int t = 0; t < PER; ++t) {
+      const uint32_t key = score_key(v[t]);
+      flags |= (uint32_t)(e0 + t < hi && key >= t_lo) << t;
+    }
+    uint32_t total;
+    uint32_t o = written + block_exclusive_scan(__popc(flags), &total, warp_buf);
+    if (written + total > (uint32_t)LCAP) {
+      overflow = true;
+      break;
+    }
+#pragma unroll
+    for (int t = 0; t < PER; ++t) {
+      if ((flags >> t) & 1u) {
+        ckey[o] = score_key(v[t]);
+        cpos[o] = (int32_t)(e0 + t);
+        ++o;
+      }
+    }
+    written += total;
+  }
+  if (tid == 0) {
+    vars[1] = written;
+    vars[2] = overflow ? 1u : 0u;
+  }
+  cluster.sync();
+
+  // ---- 3. CTA 0: gather, select exactly, write ----
+  bool fallback = false;
+  if (rank == 0) {
+    uint32_t offs[C];
+    uint32_t total = 0;
+    for (int r = 0; r < C; ++r) {
+      const uint32_t* rv = cluster.map_shared_rank(vars, r);
+      offs[r] = total;
+      total += rv[1];
+      if (rv[2]) fallback = true;
+    }
+    if (total > (uint32_t)MCAP || total < (uint32_t)k) fallback = true;
+    if (!fallback && C > 1) {
+      for (int r = 0; r < C; ++r) {
+        const uint32_t* rk = cluster.map_shared_rank(ckey, r);
+        const int32_t* rp = cluster.map_shared_rank(cpos, r);
+        const uint32_t n = *cluster.map_shared_rank(&vars[1], r);
+        for (uint32_t e = tid; e < n; e += NT) {
+          mkey[offs[r] + e] = rk[e];
+          mpos[offs[r] + e] = rp[e];
+        }
+      }
+    }
+    __syncthreads();
+    if (!fallback) vars[3] = total;
+  }
+  cluster.sync();  // the other CTAs' shared memory is no longer read
+  if (rank != 0) return;
+  if (!fallback) {
+    select_exact<false>(nullptr, mkey, mpos, vars[3], (uint32_t)k, out, hist, warp_buf, sel);
+  } else {
+    select_exact<true>(s, nullptr, nullptr, vis, (uint32_t)k, out, hist, warp_buf, sel);
+  }
+}
+
+template <int C>
+cudaError_t launch_c(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k, int32_t* idx,
+                     int32_t* dev_status, cudaStream_t stream) {
+  auto kern = topk_cluster_kernel<C>;
+  const size_t smem = TopkSmem<C>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)num_q * C, NT, smem, stream>>>(scores, ld, q_pos, k, idx, dev_status);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_topk_radix(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
-                              int32_t* idx, int32_t* dev_status, cudaStream_t stream) {
+int topk_cluster_size(int32_t num_q, int64_t ld, int num_sms) {
+  int c = 1;
+  while (c < 8 && (int64_t)num_q * c * 2 <= 2 * (int64_t)num_sms && ld / (2 * c) >= 16384) c *= 2;
+  return c;
+}
+
+cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
+                        int32_t* idx, int32_t* dev_status, cudaStream_t stream) {
   if (num_q == 0) return cudaSuccess;
-  topk_radix_kernel<<<num_q, kTopkThreads, 0, stream>>>(scores, ld, q_pos, k, idx, dev_status);
-  return cudaGetLastError();
+  const int sms = device_sm_count();
+  switch (topk_cluster_size(num_q, ld, sms)) {
+    case 8: return launch_c<8>(scores, ld, q_pos, num_q, k, idx, dev_status, stream);
+    case 4: return launch_c<4>(scores, ld, q_pos, num_q, k, idx, dev_status, stream);
+    case 2: return launch_c<2>(scores, ld, q_pos, num_q, k, idx, dev_status, stream);
+    default: return launch_c<1>(scores, ld, q_pos, num_q, k, idx, dev_status, stream);
+  }
 }
 
 }  // namespace dsa

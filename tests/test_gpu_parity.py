@@ -281,4 +281,39 @@ def test_large_logit_range_triggers_rescale():
     rows = np.arange(w.num_q)
     ref_idx, ref_out, ref_lse = oracle_rows(inp, rows)
     assert np.array_equal(host(idx), ref_idx)
-    assert_close(host(out.float()), host(lse), ref_out, ref_lse, w.name)
+    # Such peaked softmaxes give outputs as large as single value rows, so
+    # the bf16 roundings of P (relative 2^-9 per weight) and of O (relative
+    # 2^-9) bound the error by 2^-9 (max|O| + max|V|), above the absolute
+    # 1e-2 of the N(0,1) workloads; that derived bound is the check here.
+    max_v = float((inp.kv_scale.max() * 448.0).item())
+    tol = 2.0 ** -9 * (float(np.abs(ref_out).max()) + max_v)
+    got = host(out.float()).astype(np.float64)
+    assert float(np.abs(got - ref_out).max()) <= tol
+    assert float(np.linalg.norm(got - ref_out) / np.linalg.norm(ref_out)) <= REL_L2
+    assert float(np.abs(host(lse) - ref_lse).max()) <= LSE_ABS
+
+
+def test_topk_sampling_fallbacks():
+    """Rows on which the sampled threshold cannot work (all scores equal: too
+    many candidates; high scores only at unsampled positions: too few) take
+    the exact fallback and must still match the oracle bit for bit."""
+    ld, k = 70000, 2048
+    rows = []
+    rows.append(np.full(ld, 0.5, dtype=np.float32))                       # all equal
+    r = np.random.default_rng(4).standard_normal(ld).astype(np.float32)
+    pos = np.arange(ld)
+    r[(pos % 128) >= 8] += 10.0                                            # unsampled positions high
+    rows.append(r)
+    r2 = np.random.default_rng(5).standard_normal(ld).astype(np.float32)
+    r2[(pos % 128) < 8] += 10.0                                            # sampled positions high
+    rows.append(r2)
+    rows.append(np.sort(np.random.default_rng(6).standard_normal(ld).astype(np.float32))[::-1].copy())
+    scores = np.stack(rows)
+    q_pos = np.array([ld - 1, ld - 1, ld - 100, ld - 7], dtype=np.int32)
+    got = dsa.topk_select(torch.tensor(scores, device="cuda"), torch.tensor(q_pos, device="cuda"), k)
+    assert np.array_equal(host(got), oracle.topk(scores, q_pos, k))
+    # the same rows in a batch big enough to use multi-CTA clusters
+    big = np.concatenate([scores] * 2)
+    qp = np.concatenate([q_pos] * 2)
+    got = dsa.topk_select(torch.tensor(big, device="cuda"), torch.tensor(qp, device="cuda"), k)
+    assert np.array_equal(host(got), oracle.topk(big, qp, k))
