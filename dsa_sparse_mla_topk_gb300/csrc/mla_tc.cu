@@ -54,8 +54,10 @@ constexpr int NTHREADS = 512;
 constexpr int NCONV = 6;               // converter warps
 constexpr int CONV_THREADS = NCONV * 32;
 constexpr int CHUNKS_PER_KATOM = T * 4;  // 16-byte FP8 chunks per slice
-constexpr int QD = 3;                  // converter prefetch depth (slices)
-constexpr float RESCALE_LOG2 = 8.0f;
+constexpr int TILE_CHUNKS_PER_THREAD = NKA * CHUNKS_PER_KATOM / CONV_THREADS;  // 24
+static_assert(NKA * CHUNKS_PER_KATOM == TILE_CHUNKS_PER_THREAD * CONV_THREADS, "even split of a tile");
+constexpr float RESCALE_LOG2 = 8.0f;   // a slow-path tile raises a head's reference max only past 2^8
+constexpr float EXCEED_LOG2 = 32.0f;   // fast path while no logit exceeds its reference by 2^32
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -73,7 +75,7 @@ constexpr int OFF_RED = OFF_SCALE + NST * T * 4;           // 227328
 constexpr int OFF_MUSE = OFF_RED + 4 * H * 4;              // 228352
 constexpr int OFF_ALPHA = OFF_MUSE + H * 4;                // 228608
 constexpr int OFF_FLAG = OFF_ALPHA + H * 4;                // 228864
-constexpr int OFF_BAR = OFF_FLAG + 64;                     // 228928
+constexpr int OFF_BAR = OFF_FLAG + 128;                    // 228992
 // barrier indices
 constexpr int B_KV = 0;                 // [NKA] slice a of the current tile is in smem
 constexpr int B_SFULL = B_KV + NKA;     // S^T of the tile is in TMEM
@@ -84,7 +86,8 @@ constexpr int B_IFULL = B_OFULL + 1;    // [NST] index stage filled
 constexpr int B_IFREE = B_IFULL + NST;  // [NST] index stage consumed
 constexpr int B_SYNCA = B_IFREE + NST;  // softmax-group sync points
 constexpr int B_SYNCB = B_SYNCA + 1;
-constexpr int B_FINAL = B_SYNCB + 1;
+constexpr int B_SYNCC = B_SYNCB + 1;
+constexpr int B_FINAL = B_SYNCC + 1;
 constexpr int NBAR = B_FINAL + 1;
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_TMEM + 16;
@@ -199,7 +202,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
   float* red_s = reinterpret_cast<float*>(smem + OFF_RED);
   float* muse_s = reinterpret_cast<float*>(smem + OFF_MUSE);
   float* alpha_s = reinterpret_cast<float*>(smem + OFF_ALPHA);
-  int* flag_s = reinterpret_cast<int*>(smem + OFF_FLAG);
+  int* vote_s = reinterpret_cast<int*>(smem + OFF_FLAG);  // [2][8] per-tile votes (double buffered)
+  int* resc_s = vote_s + 16;                                // [2] rescale needed, per head half
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
   auto bar = [&](int b) { return smem_u32(bars + b); };
@@ -247,6 +251,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
     }
     mbar_init(bar(B_SYNCA), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCB), SOFTMAX_WARPS);
+    mbar_init(bar(B_SYNCC), SOFTMAX_WARPS);
     mbar_init(bar(B_FINAL), 1);
     fence_mbarrier_init();
   }
@@ -372,7 +377,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
     float l_part[32];
 #pragma unroll
     for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
-    uint32_t sync_phase = 0;
+    uint32_t ph_a = 0, ph_b = 0, ph_c = 0;  // completed phases of the group barriers
+    auto group_sync = [&](int b, uint32_t& ph) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(b));
+      const bool done = mbar_wait(bar(b), ph & 1);
+      ++ph;
+      return done;
+    };
+    const int sw = warp - 4;  // softmax warp 0..7
     for (int lt = 0; lt < ntl && ok; ++lt) {
       const int st = lt % NST;
       if (!mbar_wait(bar(B_IFULL + st), (lt / NST) & 1) || !mbar_wait(bar(B_SFULL), lt & 1)) {
@@ -395,61 +408,69 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
           z[h + 16] = valid ? w[h] * cj : -INFINITY;
         }
       };
-      {
-        float z[32];
-        load_z(z);
-        red_s[q4 * H + half * 32 + lane] = warp_transpose_reduce<true>(z, lane);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SYNCA));
-      if (!mbar_wait(bar(B_SYNCA), sync_phase & 1)) {
-        ok = false;
-        break;
-      }
-      if (q4 == 0) {  // warps 4 and 8 own 32 heads each
-        const int hh = half * 32 + lane;
-        const float mt = fmaxf(fmaxf(red_s[hh], red_s[H + hh]), fmaxf(red_s[2 * H + hh], red_s[3 * H + hh]));
-        const float mo = muse_s[hh];
-        float alpha = 1.f;
-        if (mt > mo + RESCALE_LOG2) {
-          alpha = (mo == -INFINITY) ? 0.f : ex2(mo - mt);
-          muse_s[hh] = mt;
-        }
-        alpha_s[hh] = alpha;
-        const unsigned need = __ballot_sync(0xffffffffu, lt > 0 && alpha != 1.f);
-        if (lane == 0) flag_s[half] = need != 0u;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SYNCB));
-      if (!mbar_wait(bar(B_SYNCB), sync_phase & 1)) {
-        ok = false;
-        break;
-      }
-      ++sync_phase;
-      const bool rescale = flag_s[half] != 0;
-      if (rescale) {
-        const float* al = alpha_s + half * 32;
-#pragma unroll
-        for (int h = 0; h < 32; ++h) l_part[h] *= al[h];
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            float o[16];
-            const uint32_t addr = t_lane + TM_O + 64 * c + half * 32 + 16 * g;
-            tmem_ld16(addr, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 16; ++h) o[h] *= al[16 * g + h];
-            tmem_st16(addr, o);
-          }
-        }
-        tmem_wait_st();
-      }
-      // probabilities, folded with the row's dequantisation scale, as bf16 P
-      // (S is still in TMEM: reload it rather than keep it live across the rescale)
       float z[32];
       load_z(z);
+      // Fast path: probabilities are taken against the heads' current
+      // reference maxima; that stays exact as long as no logit exceeds its
+      // reference by more than 2^EXCEED (no overflow anywhere).  One vote
+      // of the 8 warps decides; only then is the tile maximum reduced.
+      bool bad = false;
+#pragma unroll
+      for (int h = 0; h < 32; ++h) bad |= valid && (z[h] > muse_s[half * 32 + h] + EXCEED_LOG2);
+      const unsigned bv = __ballot_sync(0xffffffffu, bad);
+      if (lane == 0) vote_s[(lt & 1) * SOFTMAX_WARPS + sw] = bv != 0u;
+      if (!group_sync(B_SYNCA, ph_a)) {
+        ok = false;
+        break;
+      }
+      int anybad = 0;
+#pragma unroll
+      for (int w = 0; w < SOFTMAX_WARPS; ++w) anybad |= vote_s[(lt & 1) * SOFTMAX_WARPS + w];
+      if (anybad) {  // uniform over the 8 warps
+        red_s[q4 * H + half * 32 + lane] = warp_transpose_reduce<true>(z, lane);
+        if (!group_sync(B_SYNCB, ph_b)) {
+          ok = false;
+          break;
+        }
+        if (q4 == 0) {  // warps 4 and 8 own 32 heads each
+          const int hh = half * 32 + lane;
+          const float mt = fmaxf(fmaxf(red_s[hh], red_s[H + hh]), fmaxf(red_s[2 * H + hh], red_s[3 * H + hh]));
+          const float mo = muse_s[hh];
+          float alpha = 1.f;
+          if (mt > mo + RESCALE_LOG2) {
+            alpha = (mo == -INFINITY) ? 0.f : ex2(mo - mt);
+            muse_s[hh] = mt;
+          }
+          alpha_s[hh] = alpha;
+          const unsigned need = __ballot_sync(0xffffffffu, lt > 0 && alpha != 1.f);
+          if (lane == 0) resc_s[half] = need != 0u;
+        }
+        if (!group_sync(B_SYNCC, ph_c)) {
+          ok = false;
+          break;
+        }
+        if (resc_s[half]) {
+          const float* al = alpha_s + half * 32;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) l_part[h] *= al[h];
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              float o[16];
+              const uint32_t addr = t_lane + TM_O + 64 * c + half * 32 + 16 * g;
+              tmem_ld16(addr, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < 16; ++h) o[h] *= al[16 * g + h];
+              tmem_st16(addr, o);
+            }
+          }
+          tmem_wait_st();
+        }
+        load_z(z);  // S is still in TMEM: reload rather than keep z live across the rescale
+      }
+      // probabilities, folded with the row's dequantisation scale, as bf16 P
       uint32_t pk[16];
 #pragma unroll
       for (int h2 = 0; h2 < 16; ++h2) {
@@ -478,11 +499,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
     if (ok && !mbar_wait(bar(B_OFULL), 0)) ok = false;
     if (ok) {
       tc_fence_after_sync();
-      const float ws = warp_transpose_reduce<false>(l_part, lane);
-      red_s[q4 * H + half * 32 + lane] = ws;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SYNCA));
-      ok = mbar_wait(bar(B_SYNCA), sync_phase & 1);
+      red_s[q4 * H + half * 32 + lane] = warp_transpose_reduce<false>(l_part, lane);
+      ok = group_sync(B_SYNCB, ph_b);
     }
     if (ok) {
       if (q4 == 0) {
@@ -497,9 +515,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
           a.lse_part[((int64_t)split * a.num_q + i) * H + hh] = lse;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SYNCB));
-      ok = mbar_wait(bar(B_SYNCB), sync_phase & 1);
+      ok = group_sync(B_SYNCC, ph_c);
     }
     if (ok) {
       const float* inv = alpha_s + half * 32;
@@ -528,42 +544,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
     }
   } else {
     // ---------------- converter warps: gather FP8 rows, convert, store swizzled bf16 ----------------
+    // Each thread owns 24 of the tile's 4608 16-byte chunks (chunk g = ctid +
+    // 192 r lies in slice g / 512) and holds them in registers: the whole next
+    // tile is loaded while the current one is multiplied, so the gather keeps
+    // a full tile (74 KB) in flight per SM instead of waiting slice by slice.
     const int ctid = (warp < 4 ? (warp - 2) : (warp - 12 + 2)) * 32 + lane;  // 0..191
-    const int nitems = ntl * NKA;
-    uint4 buf[QD][3];
-    int loaded_lt = -1;
+    uint4 stage[TILE_CHUNKS_PER_THREAD];
 
-    auto load_item = [&](int m, uint4 (&b)[3]) {
-      const int lt = m / NKA, ka = m % NKA, st = lt % NST;
-      if (lt != loaded_lt) {
-        if (!mbar_wait(bar(B_IFULL + st), (lt / NST) & 1)) ok = false;
-        loaded_lt = lt;
-      }
+    auto load_tile = [&](int lt) {
+      const int st = lt % NST;
+      if (!mbar_wait(bar(B_IFULL + st), (lt / NST) & 1)) ok = false;
 #pragma unroll
-      for (int rr = 0; rr < 3; ++rr) {
-        const int e = ctid + CONV_THREADS * rr;
-        b[rr] = make_uint4(0u, 0u, 0u, 0u);
-        if (e < CHUNKS_PER_KATOM && ok) {
-          const int row = e >> 2, c16 = e & 3;
-          const int64_t slot = slot_s[st * T + row];
-          if (slot >= 0) b[rr] = ldg_nc(a.kv + slot * DQK + ka * 64 + c16 * 16);
-        }
+      for (int rr = 0; rr < TILE_CHUNKS_PER_THREAD; ++rr) {
+        const int g = ctid + CONV_THREADS * rr;
+        const int ka = g >> 9, e = g & 511;
+        const int row = e >> 2, c16 = e & 3;
+        const int64_t slot = ok ? slot_s[st * T + row] : -1;
+        stage[rr] = make_uint4(0u, 0u, 0u, 0u);
+        if (slot >= 0) stage[rr] = ldg_nc(a.kv + slot * DQK + ka * 64 + c16 * 16);
       }
-      if (ka == NKA - 1) {  // last slice of the tile: this warp is done with the index stage
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_IFREE + st));
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_IFREE + st));  // slots of this stage are no longer needed here
     };
 
-#pragma unroll
-    for (int u = 0; u < QD; ++u)
-      if (u < nitems) load_item(u, buf[u]);
-    for (int n = 0; n < nitems && ok; n += QD) {
-#pragma unroll
-      for (int u = 0; u < QD; ++u) {
-        const int m = n + u;
-        if (m >= nitems || !ok) break;
-        const int lt = m / NKA, ka = m % NKA;
+    if (ntl > 0) load_tile(0);
+    for (int lt = 0; lt < ntl && ok; ++lt) {
+      for (int ka = 0; ka < NKA; ++ka) {
         if (lt > 0) {
           const int c = ka < 8 ? (ka >> 1) : 3;
           if (!mbar_wait(bar(B_VFREE + c), (lt - 1) & 1)) {
@@ -573,12 +579,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
         }
         unsigned char* dst = kv_s + ka * KATOM_BYTES;
 #pragma unroll
-        for (int rr = 0; rr < 3; ++rr) {
-          const int e = ctid + CONV_THREADS * rr;
-          if (e < CHUNKS_PER_KATOM) {
+        for (int rr = 0; rr < TILE_CHUNKS_PER_THREAD; ++rr) {
+          const int g = ctid + CONV_THREADS * rr;
+          if ((g >> 9) == ka) {
+            const int e = g & 511;
             const int row = e >> 2, c16 = e & 3;
             uint4 lo, hi;
-            convert16(buf[u][rr], lo, hi);
+            convert16(stage[rr], lo, hi);
             *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16)) = lo;
             *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + 1)) = hi;
           }
@@ -586,8 +593,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_KV + ka));
-        if (m + QD < nitems) load_item(m + QD, buf[u]);
       }
+      if (ok && lt + 1 < ntl) load_tile(lt + 1);
     }
     if (!ok) report(a.dev_status, DSA_DEV_TIMEOUT);
   }

@@ -99,22 +99,45 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32
 
 // Exact selection over n keys with positions (keys/pos in any memory, in
 // ascending position order): writes the k chosen positions ascending.
+// Radix passes of up to 11 bits run over (key - kmin) from its highest set
+// bit down, so the bins spread over the keys' actual range (candidate keys
+// share their top bits; fixed digits would pile them into a few bins).
 template <bool GLOBAL_ROW>
 __device__ void select_exact(const float* row_scores, const uint32_t* keys, const int32_t* pos, int64_t n, uint32_t k,
                              int32_t* out, uint32_t* hist, uint32_t* warp_buf, uint32_t* sel) {
   auto key_at = [&](int64_t e) -> uint32_t { return GLOBAL_ROW ? score_key(row_scores[e]) : keys[e]; };
   auto pos_at = [&](int64_t e) -> int32_t { return GLOBAL_ROW ? (int32_t)e : pos[e]; };
+  uint32_t kmin = 0, top = 32;
+  if (!GLOBAL_ROW) {
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int64_t e = threadIdx.x; e < n; e += NT) {
+      const uint32_t key = keys[e];
+      lo = min(lo, key);
+      hi = max(hi, key);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+      atomicMin(&sel[2], lo);
+      atomicMax(&sel[3], hi);
+    }
+    __syncthreads();
+    kmin = sel[2];
+    const uint32_t diff = sel[3] - kmin;
+    top = 32 - __clz(diff);  // significant bits of (key - kmin); 0 when all keys are equal
+    __syncthreads();
+  }
   uint32_t prefix = 0, mask = 0, krem = k;
-  const int shifts[3] = {21, 10, 0};
-  const uint32_t dmask[3] = {0x7ffu, 0x7ffu, 0x3ffu};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass];
-    const uint32_t dm = dmask[pass];
+  while (top > 0) {
+    const int sh = top > 11 ? (int)top - 11 : 0;
+    const uint32_t dm = (1u << (top - sh)) - 1u;
     for (int b = threadIdx.x; b < 2048; b += NT) hist[b] = 0;
     __syncthreads();
     for (int64_t e = threadIdx.x; e < n; e += NT) {
-      const uint32_t key = key_at(e);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+      const uint32_t u = key_at(e) - kmin;
+      if ((u & mask) == prefix) atomicAdd(&hist[(u >> sh) & dm], 1u);
     }
     __syncthreads();
     uint32_t bin, above, count;
@@ -122,6 +145,7 @@ __device__ void select_exact(const float* row_scores, const uint32_t* keys, cons
     prefix |= bin << sh;
     mask |= dm << sh;
     krem -= above;
+    top = sh;
     if (count == krem) break;  // the whole bin is taken
   }
   // ordered output: keys above the prefix, then the first krem equal ones
@@ -133,7 +157,7 @@ __device__ void select_exact(const float* row_scores, const uint32_t* keys, cons
 #pragma unroll
     for (int t = 0; t < PER; ++t) {
       if (e0 + t < n) {
-        const uint32_t mk = key_at(e0 + t) & mask;
+        const uint32_t mk = (key_at(e0 + t) - kmin) & mask;
         gt |= (uint32_t)(mk > prefix) << t;
         eq |= (uint32_t)(mk == prefix) << t;
       }
@@ -322,6 +346,10 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 1)
     }
     __syncthreads();
     if (!fallback) vars[3] = total;
+  }
+  if (tid == 0) {
+    sel[2] = 0xffffffffu;
+    sel[3] = 0u;
   }
   cluster.sync();  // the other CTAs' shared memory is no longer read
   if (rank != 0) return;
