@@ -24,13 +24,17 @@
 //    of a head is only raised (and O, l rescaled) when a tile's max exceeds
 //    it by more than 2^8; otherwise the stale max is kept, which is exact
 //    because O and l always share the same reference.
-//  * Warp roles: warp 0 allocates TMEM and one lane issues every MMA; warp 1
-//    resolves indices -> slots and scales 4 tiles ahead and prefetches the
-//    rows into L2; 6 converter warps gather + convert rows katom by katom
-//    (64-column slices) as soon as the previous tile's MMAs release them;
-//    8 softmax warps (2 per TMEM lane quadrant, 32 heads each) turn S into
-//    P and finally write O / l.  All hand-offs are mbarriers; every wait is
-//    bounded in time and reports DSA_DEV_TIMEOUT instead of hanging.
+//  * Warp roles (18 warps): warp 0 allocates TMEM and one lane issues every
+//    MMA; warp 1 resolves indices -> slots and scales, two tiles per round
+//    and up to 4 tiles ahead, and prefetches the rows into L2; 8 gather
+//    warps hold the next tile's FP8 rows in registers (the whole tile is in
+//    flight while the current one is multiplied; 8 lanes read one 128-byte
+//    row segment, so a warp load touches only 4 cache lines), then convert
+//    and store them 128 columns at a time as the previous tile's PV MMAs
+//    release the space; 8 softmax warps (2 per TMEM lane quadrant, 32 heads
+//    each) turn S into P and finally write O / l.  All hand-offs are
+//    mbarriers; every wait is bounded in time and reports DSA_DEV_TIMEOUT
+//    instead of hanging.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -50,12 +54,14 @@ constexpr int NKA = DQK / 64;          // 64-column slices ("katoms") per row: 9
 constexpr int KATOM_BYTES = T * 128;   // one slice of the KV tile: 128 rows x 128 B
 constexpr int QATOM_BYTES = H * 128;   // one slice of Q: 64 heads x 128 B
 constexpr int NST = 4;                 // index-ring stages
-constexpr int NTHREADS = 512;
-constexpr int NCONV = 6;               // converter warps
-constexpr int CONV_THREADS = NCONV * 32;
-constexpr int CHUNKS_PER_KATOM = T * 4;  // 16-byte FP8 chunks per slice
-constexpr int TILE_CHUNKS_PER_THREAD = NKA * CHUNKS_PER_KATOM / CONV_THREADS;  // 24
-static_assert(NKA * CHUNKS_PER_KATOM == TILE_CHUNKS_PER_THREAD * CONV_THREADS, "even split of a tile");
+constexpr int NTHREADS = 576;          // 18 warps
+constexpr int NGATHER = 8;             // gather/convert warps (warps 2..9)
+constexpr int GATHER_THREADS = NGATHER * 32;
+constexpr int SOFTMAX_WARP0 = 2 + NGATHER;  // softmax warps 10..17
+// per gather thread: 4 chunks of each 128-column pair of slices + 2 rope chunks
+constexpr int PAIR_CHUNKS = T * 8 / GATHER_THREADS;   // 4
+constexpr int ROPE_CHUNKS = T * 4 / GATHER_THREADS;   // 2
+static_assert(PAIR_CHUNKS * GATHER_THREADS == T * 8 && ROPE_CHUNKS * GATHER_THREADS == T * 4, "even split of a tile");
 constexpr float RESCALE_LOG2 = 8.0f;   // a slow-path tile raises a head's reference max only past 2^8
 constexpr float EXCEED_LOG2 = 32.0f;   // fast path while no logit exceeds its reference by 2^32
 constexpr float LOG2E = 1.4426950408889634f;
@@ -77,8 +83,9 @@ constexpr int OFF_ALPHA = OFF_MUSE + H * 4;                // 228608
 constexpr int OFF_FLAG = OFF_ALPHA + H * 4;                // 228864
 constexpr int OFF_BAR = OFF_FLAG + 128;                    // 228992
 // barrier indices
-constexpr int B_KV = 0;                 // [NKA] slice a of the current tile is in smem
-constexpr int B_SFULL = B_KV + NKA;     // S^T of the tile is in TMEM
+constexpr int B_KV = 0;                 // [5] slices 2c, 2c+1 (c < 4) / slice 8 (c = 4) of the tile are in smem
+constexpr int B_QFULL = B_KV + 5;       // Q is in smem
+constexpr int B_SFULL = B_QFULL + 1;    // S^T of the tile is in TMEM
 constexpr int B_PFULL = B_SFULL + 1;    // P of the tile is in smem (and O rescaled)
 constexpr int B_VFREE = B_PFULL + 1;    // [4] PV chunk c done: slices 2c, 2c+1 (c = 3: also slice 8) free
 constexpr int B_OFULL = B_VFREE + 4;    // all MMAs of the CTA done
@@ -192,7 +199,7 @@ __device__ __forceinline__ float warp_transpose_reduce(const float (&v)[32], int
   return IS_MAX ? fmaxf(keep, got) : keep + got;
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
+__global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* kv_s = smem + OFF_KV;
@@ -240,14 +247,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int b = 0; b < NKA; ++b) mbar_init(bar(B_KV + b), NCONV);
+    for (int b = 0; b < 5; ++b) mbar_init(bar(B_KV + b), NGATHER);
+    mbar_init(bar(B_QFULL), NGATHER);
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_PFULL), SOFTMAX_WARPS);
     for (int c = 0; c < 4; ++c) mbar_init(bar(B_VFREE + c), 1);
     mbar_init(bar(B_OFULL), 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(bar(B_IFULL + s), 32);
-      mbar_init(bar(B_IFREE + s), NCONV + SOFTMAX_WARPS);
+      mbar_init(bar(B_IFREE + s), NGATHER + SOFTMAX_WARPS);
     }
     mbar_init(bar(B_SYNCA), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCB), SOFTMAX_WARPS);
@@ -259,16 +267,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
     muse_s[tid] = -INFINITY;
     alpha_s[tid] = 1.f;
   }
-  // Q of this token -> swizzled K-major slices
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK);
-    constexpr int CH = DQK / 8;
-    for (int e = tid; e < H * CH; e += NTHREADS) {
-      const int h = e / CH, cc = e % CH;
-      *reinterpret_cast<uint4*>(q_s + (cc >> 3) * QATOM_BYTES + sw128(h, cc & 7)) = src[e];
-    }
-  }
-  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -286,19 +284,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
       constexpr uint32_t ID_PV = idesc_bf16_f32(128, 64, 1, 1);
       const uint32_t kv_base = smem_u32(kv_s), q_base = smem_u32(q_s);
       const uint32_t p_base = kv_base + 8 * KATOM_BYTES;
+      if (!mbar_wait(bar(B_QFULL), 0)) ok = false;
       for (int lt = 0; lt < ntl && ok; ++lt) {
         const uint32_t par = lt & 1;
-        for (int ka = 0; ka < NKA && ok; ++ka) {
-          if (!mbar_wait(bar(B_KV + ka), par)) {
+        for (int c = 0; c < 5 && ok; ++c) {  // slices 2c, 2c+1 (c < 4), slice 8 (c = 4)
+          if (!mbar_wait(bar(B_KV + c), par)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
+          for (int ka = 2 * c; ka < (c < 4 ? 2 * c + 2 : NKA); ++ka) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc_sw128(kv_base + ka * KATOM_BYTES + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(q_base + ka * QATOM_BYTES + kk * 32, 16, 1024);
-            mma_bf16_ss(tmem + TM_S, ad, bd, ID_QK, (ka | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc_sw128(kv_base + ka * KATOM_BYTES + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(q_base + ka * QATOM_BYTES + kk * 32, 16, 1024);
+              mma_bf16_ss(tmem + TM_S, ad, bd, ID_QK, (ka | kk) != 0);
+            }
           }
         }
         if (!ok) break;
@@ -327,49 +328,55 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- index warp: positions -> slots, scales, L2 prefetch ----------------
+    // Two tiles per round: 8 rows per lane, each step's loads all in flight at once.
     const int32_t* row_idx = a.idx + (int64_t)i * a.k;
-    for (int lt = 0; lt < ntl; ++lt) {
-      const int st = lt % NST;
-      if (lt >= NST && !mbar_wait(bar(B_IFREE + st), ((lt / NST) - 1) & 1)) {
+    for (int lt0 = 0; lt0 < ntl && ok; lt0 += 2) {
+      const int nt = ntl - lt0 < 2 ? ntl - lt0 : 2;
+      for (int u = 0; u < nt; ++u) {
+        const int lt = lt0 + u;
+        if (lt >= NST && !mbar_wait(bar(B_IFREE + lt % NST), ((lt / NST) - 1) & 1)) ok = false;
+      }
+      if (!ok) {
         report(a.dev_status, DSA_DEV_TIMEOUT);
         break;
       }
-      const int tile = t_begin + lt;
+      int32_t pos[8], page[8];
 #pragma unroll
-      for (int jj = 0; jj < T / 32; ++jj) {
-        const int j = lane + 32 * jj;
-        const int e = tile * T + j;
-        int64_t slot = -1;
-        float sc = 0.f;
-        if (e < a.k && req_ok) {
-          const int32_t pos = row_idx[e];
-          if (pos < -1) {
-            report(a.dev_status, DSA_DEV_BAD_INDEX);
-          } else if (pos >= 0) {
-            const int32_t pg = pos / a.page_size;
-            if (pg >= a.bt_stride) {
-              report(a.dev_status, DSA_DEV_BAD_INDEX);
-            } else {
-              const int32_t page = a.block_table[(int64_t)r * a.bt_stride + pg];
-              if (page < 0 || page >= a.num_pages) {
-                report(a.dev_status, DSA_DEV_BAD_PAGE);
-              } else {
-                slot = (int64_t)page * a.page_size + pos % a.page_size;
-                sc = a.kv_scale[slot];
-                prefetch_l2(a.kv + slot * DQK, DQK);
-              }
-            }
-          }
-        }
-        slot_s[st * T + j] = slot;
-        scale_s[st * T + j] = sc;
+      for (int jj = 0; jj < 8; ++jj) {
+        const int u = jj >> 2;
+        const int e = (t_begin + lt0 + u) * T + lane + 32 * (jj & 3);
+        pos[jj] = (u < nt && e < a.k && req_ok) ? __ldg(row_idx + e) : -1;
       }
-      mbar_arrive(bar(B_IFULL + st));
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int32_t pg = pos[jj] >= 0 ? pos[jj] / a.page_size : 0;
+        const bool inb = pos[jj] >= 0 && pg < a.bt_stride;
+        if (pos[jj] < -1 || (pos[jj] >= 0 && !inb)) report(a.dev_status, DSA_DEV_BAD_INDEX);
+        page[jj] = inb ? __ldg(a.block_table + (int64_t)r * a.bt_stride + pg) : -1;
+        if (inb && (page[jj] < 0 || page[jj] >= a.num_pages)) {
+          report(a.dev_status, DSA_DEV_BAD_PAGE);
+          page[jj] = -1;
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int u = jj >> 2;
+        if (u < nt) {
+          const int st = (lt0 + u) % NST;
+          const int j = lane + 32 * (jj & 3);
+          const int64_t slot = page[jj] >= 0 ? (int64_t)page[jj] * a.page_size + pos[jj] % a.page_size : -1;
+          const float sc = slot >= 0 ? __ldg(a.kv_scale + slot) : 0.f;
+          if (slot >= 0) prefetch_l2(a.kv + slot * DQK, DQK);
+          slot_s[st * T + j] = slot;
+          scale_s[st * T + j] = sc;
+        }
+      }
+      for (int u = 0; u < nt; ++u) mbar_arrive(bar(B_IFULL + (lt0 + u) % NST));
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= SOFTMAX_WARP0) {
     // ---------------- softmax warps ----------------
     const int q4 = warp & 3;            // TMEM lane quadrant
-    const int half = (warp - 4) >> 2;   // heads [32 half, 32 half + 32)
+    const int half = (warp - SOFTMAX_WARP0) >> 2;  // heads [32 half, 32 half + 32)
     const int j = 32 * q4 + lane;       // KV row of the tile = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
     const float qk_scale = a.softmax_scale * LOG2E;
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
       ++ph;
       return done;
     };
-    const int sw = warp - 4;  // softmax warp 0..7
+    const int sw = warp - SOFTMAX_WARP0;  // softmax warp 0..7
     for (int lt = 0; lt < ntl && ok; ++lt) {
       const int st = lt % NST;
       if (!mbar_wait(bar(B_IFULL + st), (lt / NST) & 1) || !mbar_wait(bar(B_SFULL), lt & 1)) {
@@ -543,25 +550,53 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
       report(a.dev_status, DSA_DEV_TIMEOUT);
     }
   } else {
-    // ---------------- converter warps: gather FP8 rows, convert, store swizzled bf16 ----------------
-    // Each thread owns 24 of the tile's 4608 16-byte chunks (chunk g = ctid +
-    // 192 r lies in slice g / 512) and holds them in registers: the whole next
-    // tile is loaded while the current one is multiplied, so the gather keeps
-    // a full tile (74 KB) in flight per SM instead of waiting slice by slice.
-    const int ctid = (warp < 4 ? (warp - 2) : (warp - 12 + 2)) * 32 + lane;  // 0..191
-    uint4 stage[TILE_CHUNKS_PER_THREAD];
+    // ---------------- gather warps: FP8 rows -> registers -> bf16 swizzled tile ----------------
+    const int gtid = (warp - 2) * 32 + lane;  // 0..255
+    // Q of this token -> swizzled K-major slices (the index warp meanwhile
+    // resolves the first tiles)
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK);
+      constexpr int CH = DQK / 8;
+      uint4 qv[H * CH / GATHER_THREADS];
+#pragma unroll
+      for (int u = 0; u < H * CH / GATHER_THREADS; ++u) qv[u] = __ldg(src + gtid + GATHER_THREADS * u);
+#pragma unroll
+      for (int u = 0; u < H * CH / GATHER_THREADS; ++u) {
+        const int e = gtid + GATHER_THREADS * u;
+        const int h = e / CH, cc = e % CH;
+        *reinterpret_cast<uint4*>(q_s + (cc >> 3) * QATOM_BYTES + sw128(h, cc & 7)) = qv[u];
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QFULL));
+    }
+    // The next tile's rows, held in registers: for each pair c of 64-column
+    // slices, 4 chunks of 16 bytes (8 lanes per 128-byte row segment), and 2
+    // chunks of the rope slice.
+    uint4 pr[4][PAIR_CHUNKS];
+    uint4 rp[ROPE_CHUNKS];
 
     auto load_tile = [&](int lt) {
       const int st = lt % NST;
       if (!mbar_wait(bar(B_IFULL + st), (lt / NST) & 1)) ok = false;
 #pragma unroll
-      for (int rr = 0; rr < TILE_CHUNKS_PER_THREAD; ++rr) {
-        const int g = ctid + CONV_THREADS * rr;
-        const int ka = g >> 9, e = g & 511;
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int u = 0; u < PAIR_CHUNKS; ++u) {
+          const int e = gtid + GATHER_THREADS * u;
+          const int row = e >> 3, c8 = e & 7;
+          const int64_t slot = ok ? slot_s[st * T + row] : -1;
+          pr[c][u] = make_uint4(0u, 0u, 0u, 0u);
+          if (slot >= 0) pr[c][u] = ldg_nc(a.kv + slot * DQK + c * 128 + c8 * 16);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < ROPE_CHUNKS; ++u) {
+        const int e = gtid + GATHER_THREADS * u;
         const int row = e >> 2, c16 = e & 3;
         const int64_t slot = ok ? slot_s[st * T + row] : -1;
-        stage[rr] = make_uint4(0u, 0u, 0u, 0u);
-        if (slot >= 0) stage[rr] = ldg_nc(a.kv + slot * DQK + ka * 64 + c16 * 16);
+        rp[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (slot >= 0) rp[u] = ldg_nc(a.kv + slot * DQK + DL + c16 * 16);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_IFREE + st));  // slots of this stage are no longer needed here
@@ -569,31 +604,44 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a) {
 
     if (ntl > 0) load_tile(0);
     for (int lt = 0; lt < ntl && ok; ++lt) {
-      for (int ka = 0; ka < NKA; ++ka) {
-        if (lt > 0) {
-          const int c = ka < 8 ? (ka >> 1) : 3;
-          if (!mbar_wait(bar(B_VFREE + c), (lt - 1) & 1)) {
-            ok = false;
-            break;
-          }
-        }
-        unsigned char* dst = kv_s + ka * KATOM_BYTES;
 #pragma unroll
-        for (int rr = 0; rr < TILE_CHUNKS_PER_THREAD; ++rr) {
-          const int g = ctid + CONV_THREADS * rr;
-          if ((g >> 9) == ka) {
-            const int e = g & 511;
-            const int row = e >> 2, c16 = e & 3;
+      for (int c = 0; c < 4; ++c) {
+        // slices 2c, 2c+1 are free once PV chunk c of the previous tile is done
+        if (lt > 0 && !mbar_wait(bar(B_VFREE + c), (lt - 1) & 1)) ok = false;
+        if (ok) {
+#pragma unroll
+          for (int u = 0; u < PAIR_CHUNKS; ++u) {
+            const int e = gtid + GATHER_THREADS * u;
+            const int row = e >> 3, c8 = e & 7;
+            const int slice = 2 * c + (c8 >> 2), c16 = c8 & 3;
             uint4 lo, hi;
-            convert16(stage[rr], lo, hi);
+            convert16(pr[c][u], lo, hi);
+            unsigned char* dst = kv_s + slice * KATOM_BYTES;
             *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16)) = lo;
             *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + 1)) = hi;
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_KV + ka));
+        if (lane == 0) mbar_arrive(bar(B_KV + c));
       }
+      // slice 8 (rope; it also holds P) is free once the whole previous PV is done,
+      // which the wait on chunk 3 above already covered
+      if (ok) {
+#pragma unroll
+        for (int u = 0; u < ROPE_CHUNKS; ++u) {
+          const int e = gtid + GATHER_THREADS * u;
+          const int row = e >> 2, c16 = e & 3;
+          uint4 lo, hi;
+          convert16(rp[u], lo, hi);
+          unsigned char* dst = kv_s + 8 * KATOM_BYTES;
+          *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16)) = lo;
+          *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + 1)) = hi;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_KV + 4));
       if (ok && lt + 1 < ntl) load_tile(lt + 1);
     }
     if (!ok) report(a.dev_status, DSA_DEV_TIMEOUT);
