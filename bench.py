@@ -273,6 +273,9 @@ def bench_ours(args):
     if S > 1:
         bufs["o_part"] = torch.empty((S, w.num_q, w.heads, w.d_latent), dtype=torch.float32, device=dev)
         bufs["lse_part"] = torch.empty((S, w.num_q, w.heads), dtype=torch.float32, device=dev)
+    ws_bytes = dsa.sparse_mla_workspace_size(w.num_q, w.heads, w.d_latent, w.d_rope, w.k)
+    if ws_bytes:
+        bufs["workspace"] = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
@@ -285,11 +288,12 @@ def bench_ours(args):
             evs[1].record(stream)
         if S == 1:
             dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, num_splits=1,
-                               out=bufs["out"], lse=bufs["lse"], dev_status=status, stream=stream, **kw)
+                               out=bufs["out"], lse=bufs["lse"], workspace=bufs.get("workspace"), dev_status=status,
+                               stream=stream, **kw)
         else:
             dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, num_splits=S,
-                               o_part=bufs["o_part"], lse_part=bufs["lse_part"], dev_status=status, stream=stream,
-                               **kw)
+                               o_part=bufs["o_part"], lse_part=bufs["lse_part"], workspace=bufs.get("workspace"),
+                               dev_status=status, stream=stream, **kw)
         if evs:
             evs[2].record(stream)
         if S > 1:
@@ -396,7 +400,8 @@ def bench_ours(args):
     ns_roof = min(NOMINAL_TFLOPS * 1e12, NOMINAL_GBS * 1e9 * ai_path)
     achieved_flops = flops / (ms_per_step / 1e3)
     meas_roof = min(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9 * ai_path)
-    launches_per_step = 2 + (1 if S > 1 else 0)
+    # top-k; the attention call (tensor-core path: resolve + attention kernels); combine when split
+    launches_per_step = 1 + (2 if ws_bytes else 1) + (1 if S > 1 else 0)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:

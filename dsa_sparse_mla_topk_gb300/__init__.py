@@ -25,7 +25,7 @@ DEV_BAD_QPOS, DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/dsa.h declares.
 EXPORTED_SYMBOLS = ("dsa_status_string", "dsa_version", "dsa_topk_select", "dsa_topk_workspace_size",
-                    "dsa_sparse_mla_fwd", "dsa_combine", "dsa_kv_tile_count", "dsa_kv_tile_size",
+                    "dsa_sparse_mla_fwd", "dsa_sparse_mla_workspace_size", "dsa_combine", "dsa_kv_tile_count", "dsa_kv_tile_size",
                     "dsa_pick_num_splits")
 
 _lock = threading.Lock()
@@ -60,7 +60,9 @@ def load_library(path: str | None = None):
         lib.dsa_topk_workspace_size.argtypes = [i32, i64, i32]
         lib.dsa_topk_workspace_size.restype = sz
         lib.dsa_sparse_mla_fwd.argtypes = [vp, vp, vp, i64, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32,
-                                           f32, i32, vp, vp, vp, vp, vp, vp]
+                                           f32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+        lib.dsa_sparse_mla_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.dsa_sparse_mla_workspace_size.restype = sz
         lib.dsa_sparse_mla_fwd.restype = i32
         lib.dsa_combine.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         lib.dsa_combine.restype = i32
@@ -134,9 +136,13 @@ def topk_select(scores: torch.Tensor, q_pos: torch.Tensor, k: int, idx: torch.Te
     return idx
 
 
+def sparse_mla_workspace_size(num_q: int, heads: int, d_latent: int, d_rope: int, k: int) -> int:
+    return load_library().dsa_sparse_mla_workspace_size(num_q, heads, d_latent, d_rope, k)
+
+
 def sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, idx, *, d_latent: int, d_rope: int, page_size: int,
                    softmax_scale: float, num_splits: int = 1, out=None, lse=None, o_part=None, lse_part=None,
-                   dev_status=None, stream=None):
+                   workspace=None, dev_status=None, stream=None):
     """Partial step.  num_splits == 1: returns (out bf16, lse fp32).
     num_splits > 1: returns (o_part fp32 [S, ...], lse_part fp32 [S, ...])."""
     _check(q, "q", torch.bfloat16, 3)
@@ -159,11 +165,15 @@ def sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, idx, *, d_latent: int, d
             o_part = torch.empty((num_splits, num_q, H, d_latent), dtype=torch.float32, device=dev)
         if lse_part is None:
             lse_part = torch.empty((num_splits, num_q, H), dtype=torch.float32, device=dev)
+    ws_bytes = sparse_mla_workspace_size(num_q, H, d_latent, d_rope, idx.shape[1])
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     _call("dsa_sparse_mla_fwd", _p(q), _p(kv), _p(kv_scale), kv.shape[0] // page_size, _p(block_table),
           block_table.shape[0], block_table.shape[1], _p(q_req), _p(idx), num_q, H, d_latent, d_rope, page_size,
           idx.shape[1], float(softmax_scale), num_splits, _p(out) if num_splits == 1 else None,
           _p(lse) if num_splits == 1 else None, _p(o_part) if num_splits > 1 else None,
-          _p(lse_part) if num_splits > 1 else None, _p(dev_status), _stream(stream))
+          _p(lse_part) if num_splits > 1 else None, _p(workspace) if ws_bytes else None, ws_bytes,
+          _p(dev_status), _stream(stream))
     return (out, lse) if num_splits == 1 else (o_part, lse_part)
 
 
@@ -185,7 +195,7 @@ def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, 
                     dev_status=None, stream=None):
     """One pass of the whole path: top-k -> Partial -> Combine (when split).
     ``buffers`` (optional) holds preallocated idx / out / lse / o_part /
-    lse_part tensors.  Returns (out, lse, idx)."""
+    lse_part / workspace tensors.  Returns (out, lse, idx)."""
     b = buffers or {}
     num_q, H, _ = q.shape
     if num_splits is None:
@@ -194,10 +204,12 @@ def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, 
     if num_splits == 1:
         out, lse = sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, idx, d_latent=d_latent, d_rope=d_rope,
                                   page_size=page_size, softmax_scale=softmax_scale, num_splits=1, out=b.get("out"),
-                                  lse=b.get("lse"), dev_status=dev_status, stream=stream)
+                                  lse=b.get("lse"), workspace=b.get("workspace"), dev_status=dev_status,
+                                  stream=stream)
         return out, lse, idx
     op, lp = sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, idx, d_latent=d_latent, d_rope=d_rope,
                             page_size=page_size, softmax_scale=softmax_scale, num_splits=num_splits,
-                            o_part=b.get("o_part"), lse_part=b.get("lse_part"), dev_status=dev_status, stream=stream)
+                            o_part=b.get("o_part"), lse_part=b.get("lse_part"), workspace=b.get("workspace"),
+                            dev_status=dev_status, stream=stream)
     out, lse = combine(op, lp, out=b.get("out"), lse=b.get("lse"), stream=stream)
     return out, lse, idx

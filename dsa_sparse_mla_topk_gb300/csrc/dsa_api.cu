@@ -16,6 +16,13 @@ bool supported_shape(int32_t h, int32_t dl, int32_t dr) {
 
 dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
+// The 64-head shape runs on the tensor cores unless DSA_FORCE_SIMT=1 asks for
+// the CUDA-core kernel (used to cross-check the two on the GPU).
+bool use_tensor_cores(int32_t h, int32_t dl, int32_t dr) {
+  const char* force = getenv("DSA_FORCE_SIMT");
+  return h == 64 && dl == 512 && dr == 64 && !(force && force[0] == '1');
+}
+
 }  // namespace
 
 namespace dsa {
@@ -78,6 +85,12 @@ int32_t dsa_pick_num_splits(int32_t num_q, int32_t num_heads, int32_t d_latent, 
   return best;
 }
 
+size_t dsa_sparse_mla_workspace_size(int32_t num_q, int32_t num_heads, int32_t d_latent, int32_t d_rope,
+                                     int32_t k) {
+  if (num_q <= 0 || k <= 0 || !use_tensor_cores(num_heads, d_latent, d_rope)) return 0;
+  return dsa::mla_tc_workspace_bytes(num_q, k);
+}
+
 size_t dsa_topk_workspace_size(int32_t num_q, int64_t ld_scores, int32_t k) {
   (void)num_q, (void)ld_scores, (void)k;
   return 0;
@@ -100,12 +113,17 @@ dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_
                               const int32_t* q_req, const int32_t* idx, int32_t num_q, int32_t num_heads,
                               int32_t d_latent, int32_t d_rope, int32_t page_size, int32_t k,
                               float softmax_scale, int32_t num_splits, void* out, float* lse, float* o_part,
-                              float* lse_part, int32_t* dev_status, void* stream) {
+                              float* lse_part, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream) {
   if (num_q < 0 || k <= 0 || page_size <= 0 || num_pages <= 0 || num_req <= 0 || bt_stride <= 0)
     return DSA_ERR_INVALID_ARG;
   if (num_splits < 1 || num_splits > 64 || !isfinite(softmax_scale)) return DSA_ERR_INVALID_ARG;
   if (!supported_shape(num_heads, d_latent, d_rope)) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (num_pages > (int64_t)INT32_MAX / page_size) return DSA_ERR_UNSUPPORTED_SHAPE;
   if (num_q == 0) return DSA_OK;
+  const size_t ws_need = dsa_sparse_mla_workspace_size(num_q, num_heads, d_latent, d_rope, k);
+  if (workspace_bytes < ws_need) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 7u))) return DSA_ERR_INVALID_ARG;
   if (!q || !kv || !kv_scale || !block_table || !q_req || !idx) return DSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
   if (num_splits == 1) {
@@ -136,9 +154,8 @@ dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_
   a.o_part = o_part;
   a.lse_part = lse_part;
   a.dev_status = dev_status;
-  const char* force = getenv("DSA_FORCE_SIMT");
-  const bool simt = force && force[0] == '1';
-  if (!simt && dsa::mla_tc_supported(a)) return from_cuda(dsa::launch_mla_tc(a, static_cast<cudaStream_t>(stream)));
+  if (use_tensor_cores(num_heads, d_latent, d_rope))
+    return from_cuda(dsa::launch_mla_tc(a, workspace, static_cast<cudaStream_t>(stream)));
   return from_cuda(dsa::launch_mla_simt(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -40,8 +40,11 @@ struct MlaArgs {
 cudaError_t launch_mla_simt(const MlaArgs& a, cudaStream_t stream);
 
 // Tensor-core (tcgen05) version for (heads, d_latent, d_rope) = (64, 512, 64).
+// It first resolves every selected position into (slot, scale) in
+// `workspace` (mla_tc_workspace_bytes), then runs the attention kernel.
 bool mla_tc_supported(const MlaArgs& a);
-cudaError_t launch_mla_tc(const MlaArgs& a, cudaStream_t stream);
+size_t mla_tc_workspace_bytes(int32_t num_q, int32_t k);
+cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream);
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t num_q,
                            int32_t heads, int32_t d_v, void* out, float* lse, cudaStream_t stream);

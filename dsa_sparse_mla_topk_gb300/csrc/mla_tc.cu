@@ -24,17 +24,17 @@
 //    of a head is only raised (and O, l rescaled) when a tile's max exceeds
 //    it by more than 2^8; otherwise the stale max is kept, which is exact
 //    because O and l always share the same reference.
-//  * Warp roles (18 warps): warp 0 allocates TMEM and one lane issues every
-//    MMA; warp 1 resolves indices -> slots and scales, two tiles per round
-//    and up to 4 tiles ahead, and prefetches the rows into L2; 8 gather
-//    warps hold the next tile's FP8 rows in registers (the whole tile is in
-//    flight while the current one is multiplied; 8 lanes read one 128-byte
-//    row segment, so a warp load touches only 4 cache lines), then convert
-//    and store them 128 columns at a time as the previous tile's PV MMAs
-//    release the space; 8 softmax warps (2 per TMEM lane quadrant, 32 heads
-//    each) turn S into P and finally write O / l.  All hand-offs are
-//    mbarriers; every wait is bounded in time and reports DSA_DEV_TIMEOUT
-//    instead of hanging.
+//  * A small resolve kernel first turns every selected position into its
+//    (slot, scale) pair, fully in parallel, into caller-provided scratch.
+//  * Warp roles (16 warps): 8 gather warps hold the next tile's FP8 rows in
+//    registers (the whole tile is in flight while the current one is
+//    multiplied; 8 lanes read one 128-byte row segment, so a warp load
+//    touches only 4 cache lines), then convert and store them 128 columns at
+//    a time as the previous tile's PV MMAs release the space; 8 softmax
+//    warps (2 per TMEM lane quadrant, 32 heads each) turn S into P and
+//    finally write O / l; the first softmax warp also allocates TMEM and
+//    issues every MMA from one lane.  All hand-offs are mbarriers; every
+//    wait is bounded in time and reports DSA_DEV_TIMEOUT instead of hanging.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -53,11 +53,11 @@ constexpr int T = 128;                 // KV rows per tile
 constexpr int NKA = DQK / 64;          // 64-column slices ("katoms") per row: 9
 constexpr int KATOM_BYTES = T * 128;   // one slice of the KV tile: 128 rows x 128 B
 constexpr int QATOM_BYTES = H * 128;   // one slice of Q: 64 heads x 128 B
-constexpr int NST = 4;                 // index-ring stages
-constexpr int NTHREADS = 576;          // 18 warps
-constexpr int NGATHER = 8;             // gather/convert warps (warps 2..9)
+constexpr int NTHREADS = 512;          // 16 warps
+constexpr int NGATHER = 8;             // gather/convert warps 0..7
 constexpr int GATHER_THREADS = NGATHER * 32;
-constexpr int SOFTMAX_WARP0 = 2 + NGATHER;  // softmax warps 10..17
+constexpr int SOFTMAX_WARP0 = NGATHER; // softmax warps 8..15; warp 8 also issues the MMAs
+constexpr int SOFTMAX_WARPS = 8;
 // per gather thread: 4 chunks of each 128-column pair of slices + 2 rope chunks
 constexpr int PAIR_CHUNKS = T * 8 / GATHER_THREADS;   // 4
 constexpr int ROPE_CHUNKS = T * 4 / GATHER_THREADS;   // 2
@@ -75,13 +75,11 @@ constexpr uint32_t TM_COLS = 512;
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int OFF_KV = 0;
 constexpr int OFF_Q = OFF_KV + NKA * KATOM_BYTES;          // 147456
-constexpr int OFF_SLOT = OFF_Q + NKA * QATOM_BYTES;        // 221184
-constexpr int OFF_SCALE = OFF_SLOT + NST * T * 8;          // 225280
-constexpr int OFF_RED = OFF_SCALE + NST * T * 4;           // 227328
-constexpr int OFF_MUSE = OFF_RED + 4 * H * 4;              // 228352
-constexpr int OFF_ALPHA = OFF_MUSE + H * 4;                // 228608
-constexpr int OFF_FLAG = OFF_ALPHA + H * 4;                // 228864
-constexpr int OFF_BAR = OFF_FLAG + 128;                    // 228992
+constexpr int OFF_RED = OFF_Q + NKA * QATOM_BYTES;         // 221184
+constexpr int OFF_MUSE = OFF_RED + 4 * H * 4;
+constexpr int OFF_ALPHA = OFF_MUSE + H * 4;
+constexpr int OFF_FLAG = OFF_ALPHA + H * 4;
+constexpr int OFF_BAR = OFF_FLAG + 128;
 // barrier indices
 constexpr int B_KV = 0;                 // [5] slices 2c, 2c+1 (c < 4) / slice 8 (c = 4) of the tile are in smem
 constexpr int B_QFULL = B_KV + 5;       // Q is in smem
@@ -89,9 +87,7 @@ constexpr int B_SFULL = B_QFULL + 1;    // S^T of the tile is in TMEM
 constexpr int B_PFULL = B_SFULL + 1;    // P of the tile is in smem (and O rescaled)
 constexpr int B_VFREE = B_PFULL + 1;    // [4] PV chunk c done: slices 2c, 2c+1 (c = 3: also slice 8) free
 constexpr int B_OFULL = B_VFREE + 4;    // all MMAs of the CTA done
-constexpr int B_IFULL = B_OFULL + 1;    // [NST] index stage filled
-constexpr int B_IFREE = B_IFULL + NST;  // [NST] index stage consumed
-constexpr int B_SYNCA = B_IFREE + NST;  // softmax-group sync points
+constexpr int B_SYNCA = B_OFULL + 1;    // softmax-group sync points
 constexpr int B_SYNCB = B_SYNCA + 1;
 constexpr int B_SYNCC = B_SYNCB + 1;
 constexpr int B_FINAL = B_SYNCC + 1;
@@ -100,8 +96,6 @@ constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_TMEM + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-
-constexpr int SOFTMAX_WARPS = 8;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -199,13 +193,45 @@ __device__ __forceinline__ float warp_transpose_reduce(const float (&v)[32], int
   return IS_MAX ? fmaxf(keep, got) : keep + got;
 }
 
-__global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
+// Resolve every selected position into (slot, dequantisation scale) once,
+// fully in parallel, so that the attention kernel's gathers depend on one
+// contiguous load instead of a chain of three: idx -> block table -> scale.
+// Invalid or padding entries get slot -1; bad inputs are reported.
+__global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __restrict__ res) {
+  const int64_t n = (int64_t)a.num_q * a.k;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = e / a.k;
+    const int32_t pos = a.idx[e];
+    int32_t slot = -1;
+    float sc = 0.f;
+    if (pos < -1) {
+      report(a.dev_status, DSA_DEV_BAD_INDEX);
+    } else if (pos >= 0) {
+      const int32_t r = a.q_req[i];
+      const int32_t pg = pos / a.page_size;
+      if (r < 0 || r >= a.num_req) {
+        report(a.dev_status, DSA_DEV_BAD_PAGE);
+      } else if (pg >= a.bt_stride) {
+        report(a.dev_status, DSA_DEV_BAD_INDEX);
+      } else {
+        const int32_t page = a.block_table[(int64_t)r * a.bt_stride + pg];
+        if (page < 0 || page >= a.num_pages) {
+          report(a.dev_status, DSA_DEV_BAD_PAGE);
+        } else {
+          slot = page * a.page_size + pos % a.page_size;
+          sc = a.kv_scale[slot];
+        }
+      }
+    }
+    res[e] = make_int2(slot, __float_as_int(sc));
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, const int2* __restrict__ res) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* kv_s = smem + OFF_KV;
   unsigned char* q_s = smem + OFF_Q;
-  int64_t* slot_s = reinterpret_cast<int64_t*>(smem + OFF_SLOT);
-  float* scale_s = reinterpret_cast<float*>(smem + OFF_SCALE);
   float* red_s = reinterpret_cast<float*>(smem + OFF_RED);
   float* muse_s = reinterpret_cast<float*>(smem + OFF_MUSE);
   float* alpha_s = reinterpret_cast<float*>(smem + OFF_ALPHA);
@@ -223,6 +249,7 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
   const int t_begin = (int)((int64_t)ntiles * split / S);
   const int t_end = (int)((int64_t)ntiles * (split + 1) / S);
   const int ntl = t_end - t_begin;
+  const int2* row_res = res + (int64_t)i * a.k;
 
   if (ntl == 0) {  // an empty split: O = 0, lse = -inf
     for (int e = tid; e < H * DL; e += NTHREADS) {
@@ -242,7 +269,7 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
   }
 
   // ---------------- setup ----------------
-  if (warp == 0) {
+  if (warp == SOFTMAX_WARP0) {
     tmem_alloc(smem_u32(tmem_slot), TM_COLS);
     tmem_relinquish();
   }
@@ -253,10 +280,6 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
     mbar_init(bar(B_PFULL), SOFTMAX_WARPS);
     for (int c = 0; c < 4; ++c) mbar_init(bar(B_VFREE + c), 1);
     mbar_init(bar(B_OFULL), 1);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(bar(B_IFULL + s), 32);
-      mbar_init(bar(B_IFREE + s), NGATHER + SOFTMAX_WARPS);
-    }
     mbar_init(bar(B_SYNCA), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCB), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCC), SOFTMAX_WARPS);
@@ -271,116 +294,60 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-
-  const int r = a.q_req[i];
-  const bool req_ok = (r >= 0 && r < a.num_req);
   bool ok = true;
 
-  if (warp == 0) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      if (!req_ok) report(a.dev_status, DSA_DEV_BAD_PAGE);
-      constexpr uint32_t ID_QK = idesc_bf16_f32(128, 64, 0, 0);
-      constexpr uint32_t ID_PV = idesc_bf16_f32(128, 64, 1, 1);
-      const uint32_t kv_base = smem_u32(kv_s), q_base = smem_u32(q_s);
-      const uint32_t p_base = kv_base + 8 * KATOM_BYTES;
-      if (!mbar_wait(bar(B_QFULL), 0)) ok = false;
-      for (int lt = 0; lt < ntl && ok; ++lt) {
-        const uint32_t par = lt & 1;
-        for (int c = 0; c < 5 && ok; ++c) {  // slices 2c, 2c+1 (c < 4), slice 8 (c = 4)
-          if (!mbar_wait(bar(B_KV + c), par)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          for (int ka = 2 * c; ka < (c < 4 ? 2 * c + 2 : NKA); ++ka) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc_sw128(kv_base + ka * KATOM_BYTES + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(q_base + ka * QATOM_BYTES + kk * 32, 16, 1024);
-              mma_bf16_ss(tmem + TM_S, ad, bd, ID_QK, (ka | kk) != 0);
-            }
-          }
-        }
-        if (!ok) break;
-        mma_commit(bar(B_SFULL));
-        if (!mbar_wait(bar(B_PFULL), par)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = smem_desc_sw128(kv_base + 2 * c * KATOM_BYTES + kk * 2048, KATOM_BYTES, 1024);
-            const uint64_t bd = smem_desc_sw128(p_base + kk * 2048, KATOM_BYTES, 1024);
-            mma_bf16_ss(tmem + TM_O + 64 * c, ad, bd, ID_PV, (lt > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(B_VFREE + c));
-        }
-      }
-      mma_commit(bar(B_OFULL));
-      mma_commit(bar(B_FINAL));
-      if (!ok) report(a.dev_status, DSA_DEV_TIMEOUT);
-      // all issued MMAs must be finished before TMEM is released
-      if (!mbar_wait(bar(B_FINAL), 0)) report(a.dev_status, DSA_DEV_TIMEOUT);
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---------------- index warp: positions -> slots, scales, L2 prefetch ----------------
-    // Two tiles per round: 8 rows per lane, each step's loads all in flight at once.
-    const int32_t* row_idx = a.idx + (int64_t)i * a.k;
-    for (int lt0 = 0; lt0 < ntl && ok; lt0 += 2) {
-      const int nt = ntl - lt0 < 2 ? ntl - lt0 : 2;
-      for (int u = 0; u < nt; ++u) {
-        const int lt = lt0 + u;
-        if (lt >= NST && !mbar_wait(bar(B_IFREE + lt % NST), ((lt / NST) - 1) & 1)) ok = false;
-      }
-      if (!ok) {
-        report(a.dev_status, DSA_DEV_TIMEOUT);
-        break;
-      }
-      int32_t pos[8], page[8];
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int u = jj >> 2;
-        const int e = (t_begin + lt0 + u) * T + lane + 32 * (jj & 3);
-        pos[jj] = (u < nt && e < a.k && req_ok) ? __ldg(row_idx + e) : -1;
-      }
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int32_t pg = pos[jj] >= 0 ? pos[jj] / a.page_size : 0;
-        const bool inb = pos[jj] >= 0 && pg < a.bt_stride;
-        if (pos[jj] < -1 || (pos[jj] >= 0 && !inb)) report(a.dev_status, DSA_DEV_BAD_INDEX);
-        page[jj] = inb ? __ldg(a.block_table + (int64_t)r * a.bt_stride + pg) : -1;
-        if (inb && (page[jj] < 0 || page[jj] >= a.num_pages)) {
-          report(a.dev_status, DSA_DEV_BAD_PAGE);
-          page[jj] = -1;
-        }
-      }
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int u = jj >> 2;
-        if (u < nt) {
-          const int st = (lt0 + u) % NST;
-          const int j = lane + 32 * (jj & 3);
-          const int64_t slot = page[jj] >= 0 ? (int64_t)page[jj] * a.page_size + pos[jj] % a.page_size : -1;
-          const float sc = slot >= 0 ? __ldg(a.kv_scale + slot) : 0.f;
-          if (slot >= 0) prefetch_l2(a.kv + slot * DQK, DQK);
-          slot_s[st * T + j] = slot;
-          scale_s[st * T + j] = sc;
-        }
-      }
-      for (int u = 0; u < nt; ++u) mbar_arrive(bar(B_IFULL + (lt0 + u) % NST));
-    }
-  } else if (warp >= SOFTMAX_WARP0) {
-    // ---------------- softmax warps ----------------
-    const int q4 = warp & 3;            // TMEM lane quadrant
+  if (warp >= SOFTMAX_WARP0) {
+    // ---------------- softmax warps (warp 8 also issues the MMAs) ----------------
+    const int q4 = warp & 3;                        // TMEM lane quadrant
     const int half = (warp - SOFTMAX_WARP0) >> 2;  // heads [32 half, 32 half + 32)
-    const int j = 32 * q4 + lane;       // KV row of the tile = TMEM lane
+    const int sw = warp - SOFTMAX_WARP0;            // softmax warp 0..7
+    const bool issuer = (warp == SOFTMAX_WARP0);
+    const int j = 32 * q4 + lane;                   // KV row of the tile = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
     const float qk_scale = a.softmax_scale * LOG2E;
     unsigned char* p_row = kv_s + 8 * KATOM_BYTES;
+    const uint32_t kv_base = smem_u32(kv_s), q_base = smem_u32(q_s);
+    const uint32_t p_base = kv_base + 8 * KATOM_BYTES;
+    constexpr uint32_t ID_QK = idesc_bf16_f32(128, 64, 0, 0);
+    constexpr uint32_t ID_PV = idesc_bf16_f32(128, 64, 1, 1);
+
+    // S^T = K Q^T for tile lt, slice pair by slice pair as the gather warps fill them
+    auto issue_qk = [&](int lt) -> bool {
+      for (int c = 0; c < 5; ++c) {
+        if (!mbar_wait(bar(B_KV + c), lt & 1)) return false;
+        tc_fence_after_sync();
+        for (int ka = 2 * c; ka < (c < 4 ? 2 * c + 2 : NKA); ++ka) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc_sw128(kv_base + ka * KATOM_BYTES + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(q_base + ka * QATOM_BYTES + kk * 32, 16, 1024);
+            mma_bf16_ss(tmem + TM_S, ad, bd, ID_QK, (ka | kk) != 0);
+          }
+        }
+      }
+      mma_commit(bar(B_SFULL));
+      return true;
+    };
+    // O^T += V^T P^T for tile lt, one 128-dim chunk at a time
+    auto issue_pv = [&](int lt) {
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = smem_desc_sw128(kv_base + 2 * c * KATOM_BYTES + kk * 2048, KATOM_BYTES, 1024);
+          const uint64_t bd = smem_desc_sw128(p_base + kk * 2048, KATOM_BYTES, 1024);
+          mma_bf16_ss(tmem + TM_O + 64 * c, ad, bd, ID_PV, (lt > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_VFREE + c));
+      }
+    };
+
+    if (issuer) {
+      if (lane == 0) {
+        if (!mbar_wait(bar(B_QFULL), 0) || !issue_qk(0)) ok = false;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+
     float l_part[32];
 #pragma unroll
     for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
@@ -392,16 +359,21 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
       ++ph;
       return done;
     };
-    const int sw = warp - SOFTMAX_WARP0;  // softmax warp 0..7
+    // (slot, scale) of this thread's row, one tile ahead
+    auto row_info = [&](int lt) -> int2 {
+      const int e = (t_begin + lt) * T + j;
+      return e < a.k ? __ldg(row_res + e) : make_int2(-1, 0);
+    };
+    int2 info = row_info(0);
     for (int lt = 0; lt < ntl && ok; ++lt) {
-      const int st = lt % NST;
-      if (!mbar_wait(bar(B_IFULL + st), (lt / NST) & 1) || !mbar_wait(bar(B_SFULL), lt & 1)) {
+      const int2 info_next = lt + 1 < ntl ? row_info(lt + 1) : make_int2(-1, 0);
+      if (!mbar_wait(bar(B_SFULL), lt & 1)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const bool valid = slot_s[st * T + j] >= 0;
-      const float sc = scale_s[st * T + j];
+      const bool valid = info.x >= 0;
+      const float sc = __int_as_float(info.y);
       const float cj = sc * qk_scale;
       // logits of row j in the log2 domain (invalid rows: -inf)
       auto load_z = [&](float (&z)[32]) {
@@ -439,7 +411,7 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
           ok = false;
           break;
         }
-        if (q4 == 0) {  // warps 4 and 8 own 32 heads each
+        if (q4 == 0) {  // warps 8 and 12 own 32 heads each
           const int hh = half * 32 + lane;
           const float mt = fmaxf(fmaxf(red_s[hh], red_s[H + hh]), fmaxf(red_s[2 * H + hh], red_s[3 * H + hh]));
           const float mo = muse_s[hh];
@@ -497,10 +469,27 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(B_PFULL));
-        mbar_arrive(bar(B_IFREE + st));
+      if (lane == 0) mbar_arrive(bar(B_PFULL));
+      if (issuer) {
+        if (lane == 0) {
+          if (!mbar_wait(bar(B_PFULL), lt & 1)) {
+            ok = false;
+          } else {
+            tc_fence_after_sync();
+            issue_pv(lt);
+            if (lt + 1 < ntl && !issue_qk(lt + 1)) ok = false;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
+      info = info_next;
+    }
+    if (issuer) {
+      if (lane == 0) {
+        mma_commit(bar(B_OFULL));
+        mma_commit(bar(B_FINAL));
+      }
+      __syncwarp();
     }
     // ---------------- epilogue: normalise and write ----------------
     if (ok && !mbar_wait(bar(B_OFULL), 0)) ok = false;
@@ -549,11 +538,28 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
     } else {
       report(a.dev_status, DSA_DEV_TIMEOUT);
     }
+    // all issued MMAs must be finished before TMEM is released
+    if (issuer && lane == 0 && !mbar_wait(bar(B_FINAL), 0)) report(a.dev_status, DSA_DEV_TIMEOUT);
+    __syncwarp();
   } else {
     // ---------------- gather warps: FP8 rows -> registers -> bf16 swizzled tile ----------------
-    const int gtid = (warp - 2) * 32 + lane;  // 0..255
-    // Q of this token -> swizzled K-major slices (the index warp meanwhile
-    // resolves the first tiles)
+    const int gtid = warp * 32 + lane;  // 0..255
+    // rows of the tile this thread gathers: 4 for the slice pairs, 2 for the rope slice
+    int pr_row[PAIR_CHUNKS], rp_row[ROPE_CHUNKS];
+#pragma unroll
+    for (int u = 0; u < PAIR_CHUNKS; ++u) pr_row[u] = (gtid + GATHER_THREADS * u) >> 3;
+#pragma unroll
+    for (int u = 0; u < ROPE_CHUNKS; ++u) rp_row[u] = (gtid + GATHER_THREADS * u) >> 2;
+    auto load_slots = [&](int lt, int (&ps)[PAIR_CHUNKS], int (&rs)[ROPE_CHUNKS]) {
+      const int base = (t_begin + lt) * T;
+#pragma unroll
+      for (int u = 0; u < PAIR_CHUNKS; ++u) ps[u] = base + pr_row[u] < a.k ? __ldg(&row_res[base + pr_row[u]].x) : -1;
+#pragma unroll
+      for (int u = 0; u < ROPE_CHUNKS; ++u) rs[u] = base + rp_row[u] < a.k ? __ldg(&row_res[base + rp_row[u]].x) : -1;
+    };
+    int ps[PAIR_CHUNKS], rs[ROPE_CHUNKS];
+    load_slots(0, ps, rs);
+    // Q of this token -> swizzled K-major slices
     {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK);
       constexpr int CH = DQK / 8;
@@ -575,34 +581,25 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
     // chunks of the rope slice.
     uint4 pr[4][PAIR_CHUNKS];
     uint4 rp[ROPE_CHUNKS];
-
-    auto load_tile = [&](int lt) {
-      const int st = lt % NST;
-      if (!mbar_wait(bar(B_IFULL + st), (lt / NST) & 1)) ok = false;
+    auto load_tile = [&]() {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int u = 0; u < PAIR_CHUNKS; ++u) {
-          const int e = gtid + GATHER_THREADS * u;
-          const int row = e >> 3, c8 = e & 7;
-          const int64_t slot = ok ? slot_s[st * T + row] : -1;
+          const int c8 = (gtid + GATHER_THREADS * u) & 7;
           pr[c][u] = make_uint4(0u, 0u, 0u, 0u);
-          if (slot >= 0) pr[c][u] = ldg_nc(a.kv + slot * DQK + c * 128 + c8 * 16);
+          if (ps[u] >= 0) pr[c][u] = ldg_nc(a.kv + (int64_t)ps[u] * DQK + c * 128 + c8 * 16);
         }
       }
 #pragma unroll
       for (int u = 0; u < ROPE_CHUNKS; ++u) {
-        const int e = gtid + GATHER_THREADS * u;
-        const int row = e >> 2, c16 = e & 3;
-        const int64_t slot = ok ? slot_s[st * T + row] : -1;
+        const int c16 = (gtid + GATHER_THREADS * u) & 3;
         rp[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (slot >= 0) rp[u] = ldg_nc(a.kv + slot * DQK + DL + c16 * 16);
+        if (rs[u] >= 0) rp[u] = ldg_nc(a.kv + (int64_t)rs[u] * DQK + DL + c16 * 16);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_IFREE + st));  // slots of this stage are no longer needed here
     };
-
-    if (ntl > 0) load_tile(0);
+    load_tile();
+    if (ntl > 1) load_slots(1, ps, rs);
     for (int lt = 0; lt < ntl && ok; ++lt) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -625,8 +622,8 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_KV + c));
       }
-      // slice 8 (rope; it also holds P) is free once the whole previous PV is done,
-      // which the wait on chunk 3 above already covered
+      // slice 8 (rope; it also holds P) is free once the whole previous PV is
+      // done, which the wait on chunk 3 above already covered
       if (ok) {
 #pragma unroll
         for (int u = 0; u < ROPE_CHUNKS; ++u) {
@@ -642,7 +639,10 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_KV + 4));
-      if (ok && lt + 1 < ntl) load_tile(lt + 1);
+      if (lt + 1 < ntl) {
+        load_tile();                                // tile lt+1: data in flight during tile lt's MMAs
+        if (lt + 2 < ntl) load_slots(lt + 2, ps, rs);  // and the slots of the tile after it
+      }
     }
     if (!ok) report(a.dev_status, DSA_DEV_TIMEOUT);
   }
@@ -650,7 +650,7 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
   // ---------------- teardown ----------------
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == SOFTMAX_WARP0) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, TM_COLS);
   }
@@ -660,12 +660,22 @@ __global__ void __maxnreg__(112) mla_tc_kernel(const MlaArgs a) {
 
 bool mla_tc_supported(const MlaArgs& a) { return a.heads == H && a.d_latent == DL && a.d_rope == DR; }
 
-cudaError_t launch_mla_tc(const MlaArgs& a, cudaStream_t stream) {
+size_t mla_tc_workspace_bytes(int32_t num_q, int32_t k) { return sizeof(int2) * (size_t)num_q * (size_t)k; }
+
+cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream) {
   if (a.num_q == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  int2* res = static_cast<int2*>(workspace);
+  const int64_t n = (int64_t)a.num_q * a.k;
+  int blocks = (int)((n + 255) / 256);
+  const int cap = 64 * device_sm_count();
+  if (blocks > cap) blocks = cap;
+  resolve_kernel<<<blocks, 256, 0, stream>>>(a, res);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_q, a.num_splits);
-  mla_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(a);
+  mla_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(a, res);
   return cudaGetLastError();
 }
 

@@ -133,15 +133,27 @@ DSA_API size_t dsa_topk_workspace_size(int32_t num_q, int64_t ld_scores, int32_t
  *                KV tiles and the call writes o_part (fp32 [S, num_q, heads,
  *                d_latent]) and lse_part (fp32 [S, num_q, heads]) instead, to
  *                be merged by dsa_combine; out and lse may then be NULL.
- * Errors: see the conventions above; page ids or indices out of range set
+ *   workspace    device scratch of at least dsa_sparse_mla_workspace_size()
+ *                bytes, 8-byte aligned (NULL allowed when that size is 0).
+ *                Its contents are overwritten; no state survives the call.
+ * Errors: see the conventions above; a workspace that is too small returns
+ * DSA_ERR_WORKSPACE_TOO_SMALL; a pool of 2^31 or more token slots returns
+ * DSA_ERR_UNSUPPORTED_SHAPE; page ids or indices out of range set
  * DSA_DEV_BAD_INDEX / DSA_DEV_BAD_PAGE and that row is skipped.
  */
 DSA_API dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_scale, int64_t num_pages,
-                              const int32_t* block_table, int32_t num_req, int32_t bt_stride,
-                              const int32_t* q_req, const int32_t* idx, int32_t num_q, int32_t num_heads,
-                              int32_t d_latent, int32_t d_rope, int32_t page_size, int32_t k,
-                              float softmax_scale, int32_t num_splits, void* out, float* lse, float* o_part,
-                              float* lse_part, int32_t* dev_status, void* stream);
+                                      const int32_t* block_table, int32_t num_req, int32_t bt_stride,
+                                      const int32_t* q_req, const int32_t* idx, int32_t num_q, int32_t num_heads,
+                                      int32_t d_latent, int32_t d_rope, int32_t page_size, int32_t k,
+                                      float softmax_scale, int32_t num_splits, void* out, float* lse, float* o_part,
+                                      float* lse_part, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream);
+
+/* Scratch bytes dsa_sparse_mla_fwd needs (8 bytes per selected entry on the
+ * tensor-core path: the resolved slot and scale of each position; 0 for
+ * shapes served by the CUDA-core kernel). */
+DSA_API size_t dsa_sparse_mla_workspace_size(int32_t num_q, int32_t num_heads, int32_t d_latent, int32_t d_rope,
+                                             int32_t k);
 
 /*
  * dsa_combine -- the DSA "Combine" step: exact log-sum-exp merge of split-KV

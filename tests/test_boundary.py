@@ -85,12 +85,12 @@ MISALIGNED = VP(0x10004)
 def _fwd(lib, **over):
     a = dict(q=FAKE, kv=FAKE, kv_scale=FAKE, num_pages=4, bt=FAKE, num_req=1, bt_stride=4, q_req=FAKE, idx=FAKE,
              num_q=1, H=64, dl=512, dr=64, P=64, k=2048, scale=0.04, S=1, out=FAKE, lse=FAKE, op=None, lp=None,
-             st=None, stream=None)
+             ws=FAKE, wsb=1 << 20, st=None, stream=None)
     a.update(over)
     return lib.dsa_sparse_mla_fwd(a["q"], a["kv"], a["kv_scale"], a["num_pages"], a["bt"], a["num_req"],
                                   a["bt_stride"], a["q_req"], a["idx"], a["num_q"], a["H"], a["dl"], a["dr"], a["P"],
-                                  a["k"], a["scale"], a["S"], a["out"], a["lse"], a["op"], a["lp"], a["st"],
-                                  a["stream"])
+                                  a["k"], a["scale"], a["S"], a["out"], a["lse"], a["op"], a["lp"], a["ws"],
+                                  a["wsb"], a["st"], a["stream"])
 
 
 @pytest.mark.parametrize("over,expect", [
@@ -99,6 +99,7 @@ def _fwd(lib, **over):
     (dict(q=None), 1), (dict(kv=None), 1), (dict(idx=None), 1), (dict(out=None), 1),
     (dict(q=MISALIGNED), 1), (dict(kv=MISALIGNED), 1), (dict(scale=float("inf")), 1),
     (dict(S=4, op=None, lp=FAKE), 1), (dict(S=4, op=MISALIGNED, lp=FAKE), 1), (dict(num_pages=0), 1),
+    (dict(wsb=100), 3), (dict(ws=None), 1), (dict(ws=VP(0x10004)), 1), (dict(num_pages=1 << 26), 2),
     (dict(num_q=0), 0),
 ])
 def test_fwd_argument_checks(lib, over, expect):
@@ -129,6 +130,12 @@ def test_topk_argument_checks(lib, args, expect):
 ])
 def test_combine_argument_checks(lib, args, expect):
     assert lib.dsa_combine(*args) == expect
+
+
+def test_workspace_size(lib):
+    assert dsa.sparse_mla_workspace_size(128, 64, 512, 64, 2048) == 128 * 2048 * 8
+    assert dsa.sparse_mla_workspace_size(2, 16, 64, 16, 64) == 0
+    assert dsa.sparse_mla_workspace_size(0, 64, 512, 64, 2048) == 0
 
 
 def test_python_binding_rejects_cpu_tensors(lib):
