@@ -67,9 +67,11 @@ constexpr float EXCEED_LOG2 = 32.0f;   // fast path while no logit exceeds its r
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-// TMEM columns
-constexpr uint32_t TM_S = 0;     // S^T: 64 columns
-constexpr uint32_t TM_O = 64;    // O^T chunk c at TM_O + 64 c
+// TMEM columns.  S^T is accumulated in 4 independent partial sums over
+// disjoint parts of the 576-long contraction, so that consecutive MMAs never
+// wait on each other's accumulator; the softmax adds the 4 parts.
+constexpr uint32_t TM_S = 0;     // S^T part p at TM_S + 64 p (p = 0..3)
+constexpr uint32_t TM_O = 256;   // O^T chunk c at TM_O + 64 c
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory map (offsets from a 1024-byte aligned base)
@@ -311,34 +313,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
     constexpr uint32_t ID_QK = idesc_bf16_f32(128, 64, 0, 0);
     constexpr uint32_t ID_PV = idesc_bf16_f32(128, 64, 1, 1);
 
-    // S^T = K Q^T for tile lt, slice pair by slice pair as the gather warps fill them
+    // S^T = K Q^T for tile lt, slice pair by slice pair as the gather warps
+    // fill them.  The 16-wide steps rotate over 4 accumulators: part
+    // 2 (slice & 1) + (step & 1), i.e. (slice 2c, step 0) -> part 0,
+    // (2c+1, 0) -> 2, (2c, 1) -> 1, (2c+1, 1) -> 3, ...
     auto issue_qk = [&](int lt) -> bool {
       for (int c = 0; c < 5; ++c) {
         if (!mbar_wait(bar(B_KV + c), lt & 1)) return false;
         tc_fence_after_sync();
-        for (int ka = 2 * c; ka < (c < 4 ? 2 * c + 2 : NKA); ++ka) {
+        const int nsl = c < 4 ? 2 : 1;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+        for (int kk = 0; kk < 4; ++kk) {
+          for (int u = 0; u < nsl; ++u) {
+            const int ka = 2 * c + u;
+            const uint32_t part = 2 * u + (kk & 1);
             const uint64_t ad = smem_desc_sw128(kv_base + ka * KATOM_BYTES + kk * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(q_base + ka * QATOM_BYTES + kk * 32, 16, 1024);
-            mma_bf16_ss(tmem + TM_S, ad, bd, ID_QK, (ka | kk) != 0);
+            mma_bf16_ss(tmem + TM_S + 64 * part, ad, bd, ID_QK, (c > 0 || kk > 1) ? 1u : 0u);
           }
         }
       }
       mma_commit(bar(B_SFULL));
       return true;
     };
-    // O^T += V^T P^T for tile lt, one 128-dim chunk at a time
+    // O^T += V^T P^T for tile lt: the 4 independent 128-dim chunks are issued
+    // round robin so that consecutive MMAs never share an accumulator
     auto issue_pv = [&](int lt) {
-      for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
           const uint64_t ad = smem_desc_sw128(kv_base + 2 * c * KATOM_BYTES + kk * 2048, KATOM_BYTES, 1024);
           const uint64_t bd = smem_desc_sw128(p_base + kk * 2048, KATOM_BYTES, 1024);
           mma_bf16_ss(tmem + TM_O + 64 * c, ad, bd, ID_PV, (lt > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(B_VFREE + c));
       }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) mma_commit(bar(B_VFREE + c));
     };
 
     if (issuer) {
@@ -377,14 +388,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       const float cj = sc * qk_scale;
       // logits of row j in the log2 domain (invalid rows: -inf)
       auto load_z = [&](float (&z)[32]) {
-        float v[16], w[16];
-        tmem_ld16(t_lane + TM_S + half * 32, v);
-        tmem_ld16(t_lane + TM_S + half * 32 + 16, w);
-        tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          z[h] = valid ? v[h] * cj : -INFINITY;
-          z[h + 16] = valid ? w[h] * cj : -INFINITY;
+        for (int g = 0; g < 2; ++g) {
+          float v0[16], v1[16], v2[16], v3[16];
+          tmem_ld16(t_lane + TM_S + half * 32 + 16 * g, v0);
+          tmem_ld16(t_lane + TM_S + 64 + half * 32 + 16 * g, v1);
+          tmem_ld16(t_lane + TM_S + 128 + half * 32 + 16 * g, v2);
+          tmem_ld16(t_lane + TM_S + 192 + half * 32 + 16 * g, v3);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) z[16 * g + h] = valid ? ((v0[h] + v1[h]) + (v2[h] + v3[h])) * cj : -INFINITY;
         }
       };
       float z[32];

@@ -31,9 +31,9 @@ namespace cg = cooperative_groups;
 namespace dsa {
 namespace {
 
-constexpr int NT = 1024;          // threads per CTA
+constexpr int NT = 512;           // threads per CTA (two CTAs fit on an SM)
 constexpr int HBINS = 4096;       // histogram bins (12 key bits)
-constexpr int MCAP = 8192;        // candidates CTA 0 can hold for the final selection
+constexpr int MCAP = 6144;        // candidates CTA 0 can hold for the final selection
 constexpr int SAMPLE_SHIFT = 7;   // sample the first 8 of every 128 positions (1/16)
 
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -75,8 +75,9 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
 // (bin, count above the bin, count in the bin).
 __device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32_t krem, uint32_t* warp_buf,
                                          uint32_t* sel, uint32_t& bin, uint32_t& above, uint32_t& count) {
-  const int per = nbins / NT;  // 2 or 4 bins per thread, highest bins to thread 0
-  uint32_t c[4] = {0u, 0u, 0u, 0u};
+  const int per = nbins / NT;  // bins per thread, highest bins to thread 0
+  uint32_t c[HBINS / NT];
+  for (int t = 0; t < HBINS / NT; ++t) c[t] = 0u;
   uint32_t sum = 0;
   for (int t = 0; t < per; ++t) {
     c[t] = hist[nbins - 1 - (threadIdx.x * per + t)];
@@ -184,13 +185,14 @@ __device__ void select_exact(const float* row_scores, const uint32_t* keys, cons
 
 template <int C>
 struct TopkSmem {
-  static constexpr int LCAP = C == 1 ? MCAP : 4096;  // candidates one CTA collects
+  // candidates one CTA collects; sized so that two 1024-thread CTAs fit on an SM
+  static constexpr int LCAP = C == 1 ? MCAP : 3072;
   static constexpr size_t bytes = sizeof(uint32_t) * HBINS + (sizeof(uint32_t) + sizeof(int32_t)) * LCAP +
                                   (C > 1 ? (sizeof(uint32_t) + sizeof(int32_t)) * MCAP : 0);
 };
 
 template <int C>
-__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 1)
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
     topk_cluster_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ q_pos, int32_t k,
                         int32_t* __restrict__ idx, int32_t* status) {
   constexpr int LCAP = TopkSmem<C>::LCAP;
@@ -277,12 +279,13 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 1)
   const uint32_t t_lo = *cluster.map_shared_rank(&vars[0], 0);
 
   // ---- 2. ordered collection of the candidates (key >= T_lo) ----
+  // Positions are processed in steps of NT*PER; the loads of two steps are
+  // issued before the first is scanned, so two steps are in flight at once.
   constexpr int PER = 16;  // contiguous positions per thread per step
   uint32_t written = 0;
   bool overflow = false;
-  for (int64_t base = lo; base < hi; base += (int64_t)NT * PER) {
+  auto load_step = [&](int64_t base, float (&v)[PER]) {
     const int64_t e0 = base + (int64_t)tid * PER;
-    float v[PER];
     if (vec && e0 + PER <= hi) {
 #pragma unroll
       for (int t = 0; t < PER / 4; ++t) {
@@ -293,18 +296,15 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 1)
 #pragma unroll
       for (int t = 0; t < PER; ++t) v[t] = (e0 + t < hi) ? __ldg(s + e0 + t) : -INFINITY;
     }
+  };
+  auto scan_step = [&](int64_t base, const float (&v)[PER]) -> bool {
+    const int64_t e0 = base + (int64_t)tid * PER;
     uint32_t flags = 0;
 #pragma unroll
-    for (int t = 0; t < PER; ++t) {
-      const uint32_t key = score_key(v[t]);
-      flags |= (uint32_t)(e0 + t < hi && key >= t_lo) << t;
-    }
+    for (int t = 0; t < PER; ++t) flags |= (uint32_t)(e0 + t < hi && score_key(v[t]) >= t_lo) << t;
     uint32_t total;
     uint32_t o = written + block_exclusive_scan(__popc(flags), &total, warp_buf);
-    if (written + total > (uint32_t)LCAP) {
-      overflow = true;
-      break;
-    }
+    if (written + total > (uint32_t)LCAP) return false;
 #pragma unroll
     for (int t = 0; t < PER; ++t) {
       if ((flags >> t) & 1u) {
@@ -314,6 +314,15 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 1)
       }
     }
     written += total;
+    return true;
+  };
+  for (int64_t base = lo; base < hi && !overflow; base += 2 * (int64_t)NT * PER) {
+    float va[PER], vb[PER];
+    const int64_t base_b = base + (int64_t)NT * PER;
+    load_step(base, va);
+    if (base_b < hi) load_step(base_b, vb);
+    if (!scan_step(base, va)) overflow = true;
+    if (!overflow && base_b < hi && !scan_step(base_b, vb)) overflow = true;
   }
   if (tid == 0) {
     vars[1] = written;
