@@ -10,8 +10,9 @@
 //
 // GB300 design (one CTA = one query token x one KV split, 512 threads):
 //  * Each KV tile is 128 selected rows.  Rows are gathered through the block
-//    table from the FP8 E4M3 cache, converted exactly to bf16 and stored ONCE
-//    in shared memory in the 128-byte-swizzled K-major layout.  That single
+//    table from the FP8 E4M3 cache, converted exactly to fp16 (one cvt per
+//    two values; E4M3 is a subset of fp16) and stored ONCE in shared memory
+//    in the 128-byte-swizzled K-major layout.  That single
 //    copy is the A operand of  S^T = K Q^T  (M = 128 rows, N = 64 heads,
 //    K = 576) and, read MN-major, of  O^T = V^T P^T  (M = 4 x 128 latent
 //    dims, N = 64 heads, K = 128 rows).  Heads sit on N so every MMA has
@@ -19,11 +20,14 @@
 //  * Accumulators live in tensor memory: S^T in 64 columns, O^T in 4 x 64.
 //  * The per-token dequantisation scale s_j is applied in fp32 where it is
 //    exact to do so: to the logits of row j, and folded into P before its
-//    bf16 rounding (P'_hj = p_hj s_j), so V stays raw FP8-valued bf16.
+//    fp16 rounding (P'_hj = p_hj s_j 2^E), so V stays raw FP8-valued fp16.
+//    2^E is a per-query power of two chosen from the largest selected scale
+//    so that P' can never overflow fp16; O is multiplied back by 2^-E.
+//    Q is converted from bf16 to fp16 once per CTA.
 //  * Online softmax in the log2 domain with lazy rescaling: the running max
 //    of a head is only raised (and O, l rescaled) when a tile's max exceeds
-//    it by more than 2^8; otherwise the stale max is kept, which is exact
-//    because O and l always share the same reference.
+//    it by more than 2^8 (so p <= 256); otherwise the stale max is kept,
+//    which is exact because O and l always share the same reference.
 //  * A small resolve kernel first turns every selected position into its
 //    (slot, scale) pair, fully in parallel, into caller-provided scratch.
 //  * Warp roles (16 warps): 8 gather warps hold the next tile's FP8 rows in
@@ -63,15 +67,15 @@ constexpr int PAIR_CHUNKS = T * 8 / GATHER_THREADS;   // 4
 constexpr int ROPE_CHUNKS = T * 4 / GATHER_THREADS;   // 2
 static_assert(PAIR_CHUNKS * GATHER_THREADS == T * 8 && ROPE_CHUNKS * GATHER_THREADS == T * 4, "even split of a tile");
 constexpr float RESCALE_LOG2 = 8.0f;   // a slow-path tile raises a head's reference max only past 2^8
-constexpr float EXCEED_LOG2 = 32.0f;   // fast path while no logit exceeds its reference by 2^32
+constexpr float EXCEED_LOG2 = 8.0f;    // fast path while no logit exceeds its reference by 2^8 (p <= 256)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-// TMEM columns.  S^T is accumulated in 4 independent partial sums over
+// TMEM columns.  S^T is accumulated in 2 independent partial sums over
 // disjoint parts of the 576-long contraction, so that consecutive MMAs never
-// wait on each other's accumulator; the softmax adds the 4 parts.
-constexpr uint32_t TM_S = 0;     // S^T part p at TM_S + 64 p (p = 0..3)
-constexpr uint32_t TM_O = 256;   // O^T chunk c at TM_O + 64 c
+// wait on each other's accumulator; the softmax adds the parts.
+constexpr uint32_t TM_S = 0;     // S^T part p at TM_S + 64 p (p = 0, 1)
+constexpr uint32_t TM_O = 128;   // O^T chunk c at TM_O + 64 c
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory map (offsets from a 1024-byte aligned base)
@@ -115,26 +119,35 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// two E4M3 values (low byte first) -> two bf16 (exact)
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+// 16 E4M3 bytes -> 16 fp16 (exact) as two 16-byte chunks, one cvt per pair
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two));
-  const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
-  const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&b);
+  return h2;
+}
+__device__ __forceinline__ void convert16(const uint4& v, uint4& lo, uint4& hi) {
+  lo.x = e4m3x2_to_f16x2(v.x & 0xffffu);
+  lo.y = e4m3x2_to_f16x2(v.x >> 16);
+  lo.z = e4m3x2_to_f16x2(v.y & 0xffffu);
+  lo.w = e4m3x2_to_f16x2(v.y >> 16);
+  hi.x = e4m3x2_to_f16x2(v.z & 0xffffu);
+  hi.y = e4m3x2_to_f16x2(v.z >> 16);
+  hi.z = e4m3x2_to_f16x2(v.w & 0xffffu);
+  hi.w = e4m3x2_to_f16x2(v.w >> 16);
 }
 
-// 16 E4M3 bytes -> 16 bf16 as two 16-byte chunks
-__device__ __forceinline__ void convert16(const uint4& v, uint4& lo, uint4& hi) {
-  lo.x = e4m3x2_to_bf16x2(v.x & 0xffffu);
-  lo.y = e4m3x2_to_bf16x2(v.x >> 16);
-  lo.z = e4m3x2_to_bf16x2(v.y & 0xffffu);
-  lo.w = e4m3x2_to_bf16x2(v.y >> 16);
-  hi.x = e4m3x2_to_bf16x2(v.z & 0xffffu);
-  hi.y = e4m3x2_to_bf16x2(v.z >> 16);
-  hi.z = e4m3x2_to_bf16x2(v.w & 0xffffu);
-  hi.w = e4m3x2_to_bf16x2(v.w >> 16);
+// 8 bf16 -> 8 fp16 (exact for |x| >= 2^-14; smaller values round to fp16's
+// subnormal grid, 2^-24)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float lo = __uint_as_float(w[t] << 16), hi = __uint_as_float(w[t] & 0xffff0000u);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    o[t] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // Offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte swizzled slice.
@@ -198,8 +211,10 @@ __device__ __forceinline__ float warp_transpose_reduce(const float (&v)[32], int
 // Resolve every selected position into (slot, dequantisation scale) once,
 // fully in parallel, so that the attention kernel's gathers depend on one
 // contiguous load instead of a chain of three: idx -> block table -> scale.
-// Invalid or padding entries get slot -1; bad inputs are reported.
-__global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __restrict__ res) {
+// Invalid or padding entries get slot -1; bad inputs are reported.  It also
+// records the largest scale each query selects (for the fp16 range of P).
+__global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __restrict__ res,
+                                                      unsigned int* __restrict__ max_scale_bits) {
   const int64_t n = (int64_t)a.num_q * a.k;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = e / a.k;
@@ -222,6 +237,8 @@ __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __r
         } else {
           slot = page * a.page_size + pos % a.page_size;
           sc = a.kv_scale[slot];
+          // scales are non-negative, so their bit patterns order like the values
+          if (sc > 0.f) atomicMax(max_scale_bits + i, __float_as_uint(sc));
         }
       }
     }
@@ -229,7 +246,8 @@ __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __r
   }
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, const int2* __restrict__ res) {
+__global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, const int2* __restrict__ res,
+                                                             const unsigned int* __restrict__ max_scale_bits) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* kv_s = smem + OFF_KV;
@@ -307,16 +325,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
     const int j = 32 * q4 + lane;                   // KV row of the tile = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
     const float qk_scale = a.softmax_scale * LOG2E;
+    // P' = p s_j 2^E with p <= 256: pick E so that 256 * max_j s_j * 2^E <= 2^15
+    int p_exp = 0;
+    {
+      const float smax = __uint_as_float(max_scale_bits[i]);
+      if (smax > 0.f) {
+        int e2;
+        frexpf(smax, &e2);  // smax < 2^e2
+        p_exp = 7 - e2;
+      }
+    }
+    const float p_scale = ldexpf(1.f, p_exp);
     unsigned char* p_row = kv_s + 8 * KATOM_BYTES;
     const uint32_t kv_base = smem_u32(kv_s), q_base = smem_u32(q_s);
     const uint32_t p_base = kv_base + 8 * KATOM_BYTES;
-    constexpr uint32_t ID_QK = idesc_bf16_f32(128, 64, 0, 0);
-    constexpr uint32_t ID_PV = idesc_bf16_f32(128, 64, 1, 1);
+    constexpr uint32_t ID_QK = idesc_f16_f32(128, 64, 0, 0, 0);
+    constexpr uint32_t ID_PV = idesc_f16_f32(128, 64, 1, 1, 0);
 
     // S^T = K Q^T for tile lt, slice pair by slice pair as the gather warps
-    // fill them.  The 16-wide steps rotate over 4 accumulators: part
-    // 2 (slice & 1) + (step & 1), i.e. (slice 2c, step 0) -> part 0,
-    // (2c+1, 0) -> 2, (2c, 1) -> 1, (2c+1, 1) -> 3, ...
+    // fill them.  The 16-wide steps alternate between 2 accumulators:
+    // part = step & 1.
     auto issue_qk = [&](int lt) -> bool {
       for (int c = 0; c < 5; ++c) {
         if (!mbar_wait(bar(B_KV + c), lt & 1)) return false;
@@ -326,10 +354,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
         for (int kk = 0; kk < 4; ++kk) {
           for (int u = 0; u < nsl; ++u) {
             const int ka = 2 * c + u;
-            const uint32_t part = 2 * u + (kk & 1);
+            const uint32_t part = kk & 1;
             const uint64_t ad = smem_desc_sw128(kv_base + ka * KATOM_BYTES + kk * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(q_base + ka * QATOM_BYTES + kk * 32, 16, 1024);
-            mma_bf16_ss(tmem + TM_S + 64 * part, ad, bd, ID_QK, (c > 0 || kk > 1) ? 1u : 0u);
+            mma_f16_ss(tmem + TM_S + 64 * part, ad, bd, ID_QK, (c > 0 || u > 0 || kk > 1) ? 1u : 0u);
           }
         }
       }
@@ -345,7 +373,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
         for (int c = 0; c < 4; ++c) {
           const uint64_t ad = smem_desc_sw128(kv_base + 2 * c * KATOM_BYTES + kk * 2048, KATOM_BYTES, 1024);
           const uint64_t bd = smem_desc_sw128(p_base + kk * 2048, KATOM_BYTES, 1024);
-          mma_bf16_ss(tmem + TM_O + 64 * c, ad, bd, ID_PV, (lt > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ss(tmem + TM_O + 64 * c, ad, bd, ID_PV, (lt > 0 || kk > 0) ? 1u : 0u);
         }
       }
 #pragma unroll
@@ -390,14 +418,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       auto load_z = [&](float (&z)[32]) {
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-          float v0[16], v1[16], v2[16], v3[16];
+          float v0[16], v1[16];
           tmem_ld16(t_lane + TM_S + half * 32 + 16 * g, v0);
           tmem_ld16(t_lane + TM_S + 64 + half * 32 + 16 * g, v1);
-          tmem_ld16(t_lane + TM_S + 128 + half * 32 + 16 * g, v2);
-          tmem_ld16(t_lane + TM_S + 192 + half * 32 + 16 * g, v3);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 16; ++h) z[16 * g + h] = valid ? ((v0[h] + v1[h]) + (v2[h] + v3[h])) * cj : -INFINITY;
+          for (int h = 0; h < 16; ++h) z[16 * g + h] = valid ? (v0[h] + v1[h]) * cj : -INFINITY;
         }
       };
       float z[32];
@@ -407,8 +433,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       // reference by more than 2^EXCEED (no overflow anywhere).  One vote
       // of the 8 warps decides; only then is the tile maximum reduced.
       bool bad = false;
+      {
+        const float4* mu4 = reinterpret_cast<const float4*>(muse_s + half * 32);
 #pragma unroll
-      for (int h = 0; h < 32; ++h) bad |= valid && (z[h] > muse_s[half * 32 + h] + EXCEED_LOG2);
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 m = mu4[h4];
+          bad |= z[4 * h4] > m.x + EXCEED_LOG2;
+          bad |= z[4 * h4 + 1] > m.y + EXCEED_LOG2;
+          bad |= z[4 * h4 + 2] > m.z + EXCEED_LOG2;
+          bad |= z[4 * h4 + 3] > m.w + EXCEED_LOG2;
+        }
+        bad &= valid;
+      }
       const unsigned bv = __ballot_sync(0xffffffffu, bad);
       if (lane == 0) vote_s[(lt & 1) * SOFTMAX_WARPS + sw] = bv != 0u;
       if (!group_sync(B_SYNCA, ph_a)) {
@@ -462,17 +498,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
         }
         load_z(z);  // S is still in TMEM: reload rather than keep z live across the rescale
       }
-      // probabilities, folded with the row's dequantisation scale, as bf16 P
+      // probabilities, folded with the row's dequantisation scale and the
+      // query's power of two, as fp16 P
       uint32_t pk[16];
+      const float sp = sc * p_scale;
+      const float4* mu4 = reinterpret_cast<const float4*>(muse_s + half * 32);
 #pragma unroll
-      for (int h2 = 0; h2 < 16; ++h2) {
-        const float m0 = muse_s[half * 32 + 2 * h2], m1 = muse_s[half * 32 + 2 * h2 + 1];
-        const float p0 = valid ? ex2(z[2 * h2] - m0) : 0.f;
-        const float p1 = valid ? ex2(z[2 * h2 + 1] - m1) : 0.f;
-        l_part[2 * h2] += p0;
-        l_part[2 * h2 + 1] += p1;
-        const __nv_bfloat162 b = __floats2bfloat162_rn(p0 * sc, p1 * sc);
-        pk[h2] = *reinterpret_cast<const uint32_t*>(&b);
+      for (int h4 = 0; h4 < 8; ++h4) {
+        const float4 m = mu4[h4];
+        const float mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int h = 4 * h4 + 2 * t;
+          const float p0 = valid ? ex2(z[h] - mm[2 * t]) : 0.f;
+          const float p1 = valid ? ex2(z[h + 1] - mm[2 * t + 1]) : 0.f;
+          l_part[h] += p0;
+          l_part[h + 1] += p1;
+          const __half2 b = __floats2half2_rn(p0 * sp, p1 * sp);
+          pk[h / 2] = *reinterpret_cast<const uint32_t*>(&b);
+        }
       }
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -516,7 +560,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
         const int hh = half * 32 + lane;
         const float l = red_s[hh] + red_s[H + hh] + red_s[2 * H + hh] + red_s[3 * H + hh];
         const float m = muse_s[hh];
-        alpha_s[hh] = l > 0.f ? 1.f / l : 0.f;
+        alpha_s[hh] = l > 0.f ? ldexpf(1.f / l, -p_exp) : 0.f;
         const float lse = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
         if (S == 1) {
           if (a.lse) a.lse[(int64_t)i * H + hh] = lse;
@@ -555,7 +599,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
     if (issuer && lane == 0 && !mbar_wait(bar(B_FINAL), 0)) report(a.dev_status, DSA_DEV_TIMEOUT);
     __syncwarp();
   } else {
-    // ---------------- gather warps: FP8 rows -> registers -> bf16 swizzled tile ----------------
+    // ---------------- gather warps: FP8 rows -> registers -> fp16 swizzled tile ----------------
     const int gtid = warp * 32 + lane;  // 0..255
     // rows of the tile this thread gathers: 4 for the slice pairs, 2 for the rope slice
     int pr_row[PAIR_CHUNKS], rp_row[ROPE_CHUNKS];
@@ -583,7 +627,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       for (int u = 0; u < H * CH / GATHER_THREADS; ++u) {
         const int e = gtid + GATHER_THREADS * u;
         const int h = e / CH, cc = e % CH;
-        *reinterpret_cast<uint4*>(q_s + (cc >> 3) * QATOM_BYTES + sw128(h, cc & 7)) = qv[u];
+        *reinterpret_cast<uint4*>(q_s + (cc >> 3) * QATOM_BYTES + sw128(h, cc & 7)) = bf16x8_to_f16x8(qv[u]);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -627,8 +671,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
             uint4 lo, hi;
             convert16(pr[c][u], lo, hi);
             unsigned char* dst = kv_s + slice * KATOM_BYTES;
-            *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16)) = lo;
-            *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + 1)) = hi;
+            // Each quarter warp (8 lanes: one row, two slices) must hit 8
+            // distinct 16-byte bank groups: lanes of the second slice store
+            // their odd chunk first.
+            const bool odd_first = c8 & 4;
+            *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + (odd_first ? 1 : 0))) = odd_first ? hi : lo;
+            *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + (odd_first ? 0 : 1))) = odd_first ? lo : hi;
           }
         }
         fence_proxy_async_smem();
@@ -673,22 +721,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
 
 bool mla_tc_supported(const MlaArgs& a) { return a.heads == H && a.d_latent == DL && a.d_rope == DR; }
 
-size_t mla_tc_workspace_bytes(int32_t num_q, int32_t k) { return sizeof(int2) * (size_t)num_q * (size_t)k; }
+size_t mla_tc_workspace_bytes(int32_t num_q, int32_t k) {
+  // resolved (slot, scale) per entry, then the largest scale per query
+  return sizeof(int2) * (size_t)num_q * (size_t)k + sizeof(int2) * (((size_t)num_q + 1) / 2);
+}
 
 cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream) {
   if (a.num_q == 0) return cudaSuccess;
   int2* res = static_cast<int2*>(workspace);
+  unsigned int* max_bits = reinterpret_cast<unsigned int*>(res + (size_t)a.num_q * a.k);
+  cudaError_t e = cudaMemsetAsync(max_bits, 0, sizeof(unsigned int) * (size_t)a.num_q, stream);
+  if (e != cudaSuccess) return e;
   const int64_t n = (int64_t)a.num_q * a.k;
   int blocks = (int)((n + 255) / 256);
   const int cap = 64 * device_sm_count();
   if (blocks > cap) blocks = cap;
-  resolve_kernel<<<blocks, 256, 0, stream>>>(a, res);
-  cudaError_t e = cudaGetLastError();
+  resolve_kernel<<<blocks, 256, 0, stream>>>(a, res, max_bits);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_q, a.num_splits);
-  mla_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(a, res);
+  mla_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(a, res, max_bits);
   return cudaGetLastError();
 }
 

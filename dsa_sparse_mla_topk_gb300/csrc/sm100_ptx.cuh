@@ -127,12 +127,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, shape M x N,
-// A/B major-ness (0 = K-major, 1 = MN-major).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+// Instruction descriptor of kind::f16: A and B both bf16 (ab_bf16 = 1) or
+// both fp16 (0), fp32 D, shape M x N, A/B major-ness (0 = K-major, 1 =
+// MN-major).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major, int ab_bf16) {
   return (1u << 4)                         // D format: f32
-         | (1u << 7)                       // A format: bf16
-         | (1u << 10)                      // B format: bf16
+         | ((uint32_t)ab_bf16 << 7)        // A format: f16 (0) / bf16 (1)
+         | ((uint32_t)ab_bf16 << 10)       // B format: same as A
          | ((uint32_t)a_mn_major << 15)    // A major
          | ((uint32_t)b_mn_major << 16)    // B major
          | ((uint32_t)(N >> 3) << 17)      // N / 8
@@ -140,7 +141,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
 }
 
 // D(tmem) (+)= A(smem desc) * B(smem desc), issued by a single thread.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
