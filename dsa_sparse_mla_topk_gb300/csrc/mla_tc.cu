@@ -215,9 +215,12 @@ __device__ __forceinline__ float warp_transpose_reduce(const float (&v)[32], int
 // records the largest scale each query selects (for the fp16 range of P).
 __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __restrict__ res,
                                                       unsigned int* __restrict__ max_scale_bits) {
-  const int64_t n = (int64_t)a.num_q * a.k;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t i = e / a.k;
+  // block (x, y): entries [256 x, 256 x + 256) of query y
+  const int64_t i = blockIdx.y;
+  const int j = blockIdx.x * 256 + threadIdx.x;
+  float smax = 0.f;
+  if (j < a.k) {
+    const int64_t e = i * a.k + j;
     const int32_t pos = a.idx[e];
     int32_t slot = -1;
     float sc = 0.f;
@@ -237,12 +240,23 @@ __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __r
         } else {
           slot = page * a.page_size + pos % a.page_size;
           sc = a.kv_scale[slot];
-          // scales are non-negative, so their bit patterns order like the values
-          if (sc > 0.f) atomicMax(max_scale_bits + i, __float_as_uint(sc));
+          smax = sc;
         }
       }
     }
     res[e] = make_int2(slot, __float_as_int(sc));
+  }
+  // the block's largest scale, then one atomic per block; scales are
+  // non-negative, so their bit patterns order like the values
+  __shared__ float wmax[8];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = smax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = wmax[0];
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, wmax[w]);
+    if (m > 0.f) atomicMax(max_scale_bits + i, __float_as_uint(m));
   }
 }
 
@@ -732,11 +746,8 @@ cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream
   unsigned int* max_bits = reinterpret_cast<unsigned int*>(res + (size_t)a.num_q * a.k);
   cudaError_t e = cudaMemsetAsync(max_bits, 0, sizeof(unsigned int) * (size_t)a.num_q, stream);
   if (e != cudaSuccess) return e;
-  const int64_t n = (int64_t)a.num_q * a.k;
-  int blocks = (int)((n + 255) / 256);
-  const int cap = 64 * device_sm_count();
-  if (blocks > cap) blocks = cap;
-  resolve_kernel<<<blocks, 256, 0, stream>>>(a, res, max_bits);
+  const dim3 rgrid((a.k + 255) / 256, a.num_q);
+  resolve_kernel<<<rgrid, 256, 0, stream>>>(a, res, max_bits);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
