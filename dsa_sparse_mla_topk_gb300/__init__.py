@@ -25,7 +25,8 @@ DEV_BAD_QPOS, DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/dsa.h declares.
 EXPORTED_SYMBOLS = ("dsa_status_string", "dsa_version", "dsa_topk_select", "dsa_topk_workspace_size",
-                    "dsa_sparse_mla_fwd", "dsa_sparse_mla_workspace_size", "dsa_combine", "dsa_kv_tile_count", "dsa_kv_tile_size",
+                    "dsa_sparse_mla_fwd", "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_fwd_noalloc",
+                    "dsa_combine", "dsa_kv_tile_count", "dsa_kv_tile_size",
                     "dsa_pick_num_splits")
 
 _lock = threading.Lock()
@@ -61,6 +62,9 @@ def load_library(path: str | None = None):
         lib.dsa_topk_workspace_size.restype = sz
         lib.dsa_sparse_mla_fwd.argtypes = [vp, vp, vp, i64, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                            f32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+        lib.dsa_sparse_mla_fwd_noalloc.argtypes = [vp, vp, vp, i64, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32,
+                                                   i32, f32, i32, vp, vp, vp, vp, vp, vp]
+        lib.dsa_sparse_mla_fwd_noalloc.restype = i32
         lib.dsa_sparse_mla_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.dsa_sparse_mla_workspace_size.restype = sz
         lib.dsa_sparse_mla_fwd.restype = i32
@@ -175,6 +179,22 @@ def sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, idx, *, d_latent: int, d
           _p(lse_part) if num_splits > 1 else None, _p(workspace) if ws_bytes else None, ws_bytes,
           _p(dev_status), _stream(stream))
     return (out, lse) if num_splits == 1 else (o_part, lse_part)
+
+
+def sparse_mla_fwd_noalloc(q, kv, kv_scale, block_table, q_req, idx, out, lse, *, d_latent: int, d_rope: int,
+                           page_size: int, softmax_scale: float, dev_status=None, stream=None):
+    """Partial step without a workspace (no device allocation inside the
+    library call): scratch comes from a fixed array in the library; the
+    caller provides out / lse.  See include/dsa.h for its limits."""
+    for t, name, dt in ((q, "q", torch.bfloat16), (kv, "kv", torch.uint8), (kv_scale, "kv_scale", torch.float32),
+                        (block_table, "block_table", torch.int32), (q_req, "q_req", torch.int32),
+                        (idx, "idx", torch.int32), (out, "out", torch.bfloat16), (lse, "lse", torch.float32)):
+        _check(t, name, dt)
+    num_q, H, _ = q.shape
+    _call("dsa_sparse_mla_fwd_noalloc", _p(q), _p(kv), _p(kv_scale), kv.shape[0] // page_size, _p(block_table),
+          block_table.shape[0], block_table.shape[1], _p(q_req), _p(idx), num_q, H, d_latent, d_rope, page_size,
+          idx.shape[1], float(softmax_scale), 1, _p(out), _p(lse), None, None, _p(dev_status), _stream(stream))
+    return out, lse
 
 
 def combine(o_part: torch.Tensor, lse_part: torch.Tensor, out=None, lse=None, stream=None):

@@ -156,6 +156,33 @@ DSA_API size_t dsa_sparse_mla_workspace_size(int32_t num_q, int32_t num_heads, i
                                              int32_t k);
 
 /*
+ * dsa_sparse_mla_fwd_noalloc -- dsa_sparse_mla_fwd for callers that cannot
+ * allocate device memory.  The pages describe no such call; it exists for
+ * callers such as serving loops that reserve all device memory at start-up
+ * and forbid later allocations (cudaMalloc can synchronise the device), or
+ * plug-in hosts that offer no allocator.
+ *
+ * Same arguments, layouts, results and errors as dsa_sparse_mla_fwd, minus
+ * the workspace: the scratch lives in a fixed 24 MiB array of device memory
+ * inside the library (one per GPU, held until the process exits).  Only the
+ * tensor-core shape (64, 512, 64) is accepted.  Calls needing more than 24
+ * MiB of scratch (dsa_sparse_mla_workspace_size) return
+ * DSA_ERR_WORKSPACE_TOO_SMALL without launching anything.  All calls share
+ * the array: calls whose GPU work overlaps (unordered streams, concurrent
+ * host threads) race and must be serialised by the caller.  The first call on
+ * a device, made with that device current, looks up the array's device
+ * address; make it before any stream capture on that device.  The call
+ * allocates nothing.
+ */
+DSA_API dsa_status dsa_sparse_mla_fwd_noalloc(const void* q, const uint8_t* kv, const float* kv_scale,
+                                              int64_t num_pages, const int32_t* block_table, int32_t num_req,
+                                              int32_t bt_stride, const int32_t* q_req, const int32_t* idx,
+                                              int32_t num_q, int32_t num_heads, int32_t d_latent, int32_t d_rope,
+                                              int32_t page_size, int32_t k, float softmax_scale, int32_t num_splits,
+                                              void* out, float* lse, float* o_part, float* lse_part,
+                                              int32_t* dev_status, void* stream);
+
+/*
  * dsa_combine -- the DSA "Combine" step: exact log-sum-exp merge of split-KV
  * partial results.  [LMSYS] section 3: KV splits add intermediate writes and
  * Combine work.
