@@ -115,8 +115,8 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // 16 E4M3 bytes -> 16 fp16 (exact) as two 16-byte chunks, one cvt per pair
@@ -716,7 +716,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       if (lane == 0) mbar_arrive(bar(B_KV + 4));
       if (lt + 1 < ntl) {
         load_tile();                                // tile lt+1: data in flight during tile lt's MMAs
-        if (lt + 2 < ntl) load_slots(lt + 2, ps, rs);  // and the slots of the tile after it
+        if (lt + 2 < ntl) {
+          load_slots(lt + 2, ps, rs);               // the slots of the tile after it,
+          // and its rows pulled into L2 (one 128-byte line per 8 lanes)
+          if ((gtid & 7) == 0) {
+#pragma unroll
+            for (int u = 0; u < PAIR_CHUNKS; ++u)
+              if (ps[u] >= 0)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) prefetch_line_l2(a.kv + (int64_t)ps[u] * DQK + c * 128);
+          }
+          if ((gtid & 3) == 0) {
+#pragma unroll
+            for (int u = 0; u < ROPE_CHUNKS; ++u)
+              if (rs[u] >= 0) prefetch_line_l2(a.kv + (int64_t)rs[u] * DQK + DL);
+          }
+        }
       }
     }
     if (!ok) report(a.dev_status, DSA_DEV_TIMEOUT);

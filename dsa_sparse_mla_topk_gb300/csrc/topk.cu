@@ -240,10 +240,13 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
   __syncthreads();
   uint32_t nsampled = 0;
   for (int64_t blk = lo + (int64_t)tid * 128; blk < hi; blk += (int64_t)NT * 128) {
+    float v[8];  // all 8 loads in flight before the first atomic
+#pragma unroll
+    for (int t = 0; t < 8; ++t) v[t] = blk + t < hi ? __ldg(s + blk + t) : 0.f;
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       if (blk + t < hi) {
-        atomicAdd(&hist[score_key(__ldg(s + blk + t)) >> 20], 1u);
+        atomicAdd(&hist[score_key(v[t]) >> 20], 1u);
         ++nsampled;
       }
     }
@@ -259,7 +262,11 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
     // the sample above it exceeds its expected share of the top k by 25% + 16
     for (int r = 1; r < C; ++r) {
       const uint32_t* rh = cluster.map_shared_rank(hist, r);
-      for (int b = tid; b < HBINS; b += NT) hist[b] += rh[b];
+      uint32_t rv[HBINS / NT];  // all remote reads in flight before the adds
+#pragma unroll
+      for (int t = 0; t < HBINS / NT; ++t) rv[t] = rh[tid + NT * t];
+#pragma unroll
+      for (int t = 0; t < HBINS / NT; ++t) hist[tid + NT * t] += rv[t];
     }
     uint32_t ns = vars[3];
     for (int r = 1; r < C; ++r) ns += *cluster.map_shared_rank(&vars[3], r);
@@ -383,8 +390,12 @@ cudaError_t launch_c(const float* scores, int64_t ld, const int32_t* q_pos, int3
 }  // namespace
 
 int topk_cluster_size(int32_t num_q, int64_t ld, int num_sms) {
+  // One CTA per row once the rows alone give half the SMs work; otherwise
+  // split long rows over a cluster until about one CTA per SM, keeping
+  // slices of at least 64K positions.
   int c = 1;
-  while (c < 8 && (int64_t)num_q * c * 2 <= 2 * (int64_t)num_sms && ld / (2 * c) >= 16384) c *= 2;
+  if ((int64_t)num_q * 2 >= num_sms) return 1;
+  while (c < 8 && (int64_t)num_q * c * 2 <= (int64_t)num_sms && ld / (2 * c) >= 65536) c *= 2;
   return c;
 }
 
