@@ -60,7 +60,7 @@ int32_t dsa_kv_tile_count(int32_t width, int32_t tile) {
 
 int32_t dsa_kv_tile_size(int32_t num_heads, int32_t d_latent, int32_t d_rope) {
   if (!supported_shape(num_heads, d_latent, d_rope)) return -1;
-  return num_heads == 64 ? 128 : 32;  // tensor-core kernel: 128-row tiles; CUDA-core kernel: 32
+  return num_heads == 64 ? 64 : 32;  // tensor-core kernel: 64-row tiles; CUDA-core kernel: 32
 }
 
 int32_t dsa_pick_num_splits(int32_t num_q, int32_t num_heads, int32_t d_latent, int32_t d_rope, int32_t k,
@@ -72,14 +72,17 @@ int32_t dsa_pick_num_splits(int32_t num_q, int32_t num_heads, int32_t d_latent, 
   if (num_q >= num_sms) return 1;
   // One CTA per SM (shared memory bound); a launch takes ceil(CTAs / SMs)
   // waves of ceil(tiles / S) tiles each, plus a fixed per-CTA cost (start-up,
-  // epilogue) of about two tiles and one more for the Combine when split.
+  // pipeline fill, epilogue: about four 64-row tiles on the tensor-core
+  // kernel, two 32-row tiles on the CUDA-core one) and one tile more for the
+  // Combine when split.
   const int32_t ntiles = dsa_kv_tile_count(k, tile);
+  const int64_t fixed = tile == 64 ? 4 : 2;
   int32_t best = 1;
   int64_t best_cost = -1;
   for (int32_t s = 1; s <= 64 && s <= ntiles; ++s) {
     const int64_t waves = ((int64_t)num_q * s + num_sms - 1) / num_sms;
     const int64_t per = (ntiles + s - 1) / s;
-    const int64_t cost = waves * (per + 2) + (s > 1 ? 1 : 0);
+    const int64_t cost = waves * (per + fixed) + (s > 1 ? 1 : 0);
     if (best_cost < 0 || cost < best_cost) best = s, best_cost = cost;
   }
   return best;

@@ -9,15 +9,17 @@
 // shared by all 64 heads of a query token.
 //
 // GB300 design (one CTA = one query token x one KV split, 512 threads):
-//  * Each KV tile is 128 selected rows.  Rows are gathered through the block
-//    table from the FP8 E4M3 cache, converted exactly to fp16 (one cvt per
-//    two values; E4M3 is a subset of fp16) and stored ONCE in shared memory
-//    in the 128-byte-swizzled K-major layout.  That single
-//    copy is the A operand of  S^T = K Q^T  (M = 128 rows, N = 64 heads,
-//    K = 576) and, read MN-major, of  O^T = V^T P^T  (M = 4 x 128 latent
-//    dims, N = 64 heads, K = 128 rows).  Heads sit on N so every MMA has
-//    M = 128 and the full tensor-core datapath is used.
-//  * Accumulators live in tensor memory: S^T in 64 columns, O^T in 4 x 64.
+//  * Each KV tile is 64 selected rows, and two tiles are resident (double
+//    buffering): while one is multiplied the next is gathered.  Rows are
+//    gathered through the block table from the FP8 E4M3 cache, converted
+//    exactly to fp16 (one cvt per two values; E4M3 is a subset of fp16) and
+//    stored ONCE in shared memory in the 128-byte-swizzled K-major layout.
+//    That single copy is the A operand of  S^T = K Q^T  (M = 64 rows, N = 64
+//    heads, K = 576) and, read MN-major, of  O^T = V^T P^T  (M = 4 x 128
+//    latent dims, N = 64 heads, K = 64 rows).  Heads sit on N: one gathered
+//    row serves every head.
+//  * Accumulators live in tensor memory: S^T per buffer, O^T in 4 x 64
+//    columns.
 //  * The per-token dequantisation scale s_j is applied in fp32 where it is
 //    exact to do so: to the logits of row j, and folded into P before its
 //    fp16 rounding (P'_hj = p_hj s_j 2^E), so V stays raw FP8-valued fp16.
@@ -53,51 +55,55 @@ namespace {
 using namespace sm100;
 
 constexpr int H = 64, DL = 512, DR = 64, DQK = DL + DR;
-constexpr int T = 128;                 // KV rows per tile
+constexpr int T = 64;                  // KV rows per tile (two tiles are resident: double buffering)
 constexpr int NKA = DQK / 64;          // 64-column slices ("katoms") per row: 9
-constexpr int KATOM_BYTES = T * 128;   // one slice of the KV tile: 128 rows x 128 B
+constexpr int KATOM_BYTES = T * 128;   // one slice of a KV tile: 64 rows x 128 B
+constexpr int TILE_BYTES = NKA * KATOM_BYTES;
 constexpr int QATOM_BYTES = H * 128;   // one slice of Q: 64 heads x 128 B
 constexpr int NTHREADS = 512;          // 16 warps
-constexpr int NGATHER = 8;             // gather/convert warps 0..7
+constexpr int NGATHER = 8;             // gather/convert warps 0..7; warp 0 also issues Q K^T
 constexpr int GATHER_THREADS = NGATHER * 32;
-constexpr int SOFTMAX_WARP0 = NGATHER; // softmax warps 8..15; warp 8 also issues the MMAs
+constexpr int SOFTMAX_WARP0 = NGATHER; // softmax warps 8..15; warp 8 also issues P V
 constexpr int SOFTMAX_WARPS = 8;
-// per gather thread: 4 chunks of each 128-column pair of slices + 2 rope chunks
-constexpr int PAIR_CHUNKS = T * 8 / GATHER_THREADS;   // 4
-constexpr int ROPE_CHUNKS = T * 4 / GATHER_THREADS;   // 2
+// per gather thread and tile: 2 chunks of each 128-column pair of slices + 1 rope chunk
+constexpr int PAIR_CHUNKS = T * 8 / GATHER_THREADS;   // 2
+constexpr int ROPE_CHUNKS = T * 4 / GATHER_THREADS;   // 1
 static_assert(PAIR_CHUNKS * GATHER_THREADS == T * 8 && ROPE_CHUNKS * GATHER_THREADS == T * 4, "even split of a tile");
 constexpr float RESCALE_LOG2 = 8.0f;   // a slow-path tile raises a head's reference max only past 2^8
 constexpr float EXCEED_LOG2 = 8.0f;    // fast path while no logit exceeds its reference by 2^8 (p <= 256)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-// TMEM columns.  S^T is accumulated in 2 independent partial sums over
-// disjoint parts of the 576-long contraction, so that consecutive MMAs never
-// wait on each other's accumulator; the softmax adds the parts.
-constexpr uint32_t TM_S = 0;     // S^T part p at TM_S + 64 p (p = 0, 1)
-constexpr uint32_t TM_O = 128;   // O^T chunk c at TM_O + 64 c
+// TMEM columns.  S^T of a tile is an M = 64 accumulator: row r of the tile
+// lives in lane 32 (r / 16) + r % 16, columns = heads.  Each of the two tile
+// buffers has its own S^T, accumulated in 2 independent partial sums over
+// disjoint parts of the contraction (consecutive MMAs never share an
+// accumulator); the softmax adds the parts.  O^T (M = 128) uses all lanes.
+constexpr uint32_t TM_S = 0;     // S^T of buffer b, part p at TM_S + 64 (2 b + p)
+constexpr uint32_t TM_O = 256;   // O^T chunk c at TM_O + 64 c
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr int OFF_KV = 0;
-constexpr int OFF_Q = OFF_KV + NKA * KATOM_BYTES;          // 147456
+constexpr int OFF_KV = 0;                                  // 2 tile buffers
+constexpr int OFF_Q = OFF_KV + 2 * TILE_BYTES;             // 147456
 constexpr int OFF_RED = OFF_Q + NKA * QATOM_BYTES;         // 221184
 constexpr int OFF_MUSE = OFF_RED + 4 * H * 4;
 constexpr int OFF_ALPHA = OFF_MUSE + H * 4;
 constexpr int OFF_FLAG = OFF_ALPHA + H * 4;
 constexpr int OFF_BAR = OFF_FLAG + 128;
 // barrier indices
-constexpr int B_KV = 0;                 // [5] slices 2c, 2c+1 (c < 4) / slice 8 (c = 4) of the tile are in smem
-constexpr int B_QFULL = B_KV + 5;       // Q is in smem
-constexpr int B_SFULL = B_QFULL + 1;    // S^T of the tile is in TMEM
-constexpr int B_PFULL = B_SFULL + 1;    // P of the tile is in smem (and O rescaled)
-constexpr int B_VFREE = B_PFULL + 1;    // [4] PV chunk c done: slices 2c, 2c+1 (c = 3: also slice 8) free
-constexpr int B_OFULL = B_VFREE + 4;    // all MMAs of the CTA done
+constexpr int B_KV = 0;                 // [2] the tile in buffer b is in smem
+constexpr int B_QFULL = B_KV + 2;       // Q is in smem
+constexpr int B_SFULL = B_QFULL + 1;    // [2] S^T of the tile in buffer b is in TMEM
+constexpr int B_PFULL = B_SFULL + 2;    // P of the current tile is in smem (and O rescaled)
+constexpr int B_BFREE = B_PFULL + 1;    // [2] P V of the tile in buffer b is done: buffer free
+constexpr int B_OFULL = B_BFREE + 2;    // all P V MMAs done
 constexpr int B_SYNCA = B_OFULL + 1;    // softmax-group sync points
 constexpr int B_SYNCB = B_SYNCA + 1;
 constexpr int B_SYNCC = B_SYNCB + 1;
-constexpr int B_FINAL = B_SYNCC + 1;
-constexpr int NBAR = B_FINAL + 1;
+constexpr int B_FINQ = B_SYNCC + 1;     // the Q K^T issuer's MMAs are done
+constexpr int B_FINP = B_FINQ + 1;      // the P V issuer's MMAs are done
+constexpr int NBAR = B_FINP + 1;
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_TMEM + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
@@ -113,10 +119,6 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
-}
-
-__device__ __forceinline__ void prefetch_line_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // 16 E4M3 bytes -> 16 fp16 (exact) as two 16-byte chunks, one cvt per pair
@@ -274,6 +276,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
   auto bar = [&](int b) { return smem_u32(bars + b); };
+  // a bounded wait whose outcome is the same for every lane of the warp
+  auto wait_warp = [&](int b, uint32_t parity) { return __all_sync(0xffffffffu, mbar_wait(bar(b), parity)); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i = blockIdx.x;        // query token
@@ -308,16 +312,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int b = 0; b < 5; ++b) mbar_init(bar(B_KV + b), NGATHER);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_KV + b), NGATHER);
+      mbar_init(bar(B_SFULL + b), 1);
+      mbar_init(bar(B_BFREE + b), 1);
+    }
     mbar_init(bar(B_QFULL), NGATHER);
-    mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_PFULL), SOFTMAX_WARPS);
-    for (int c = 0; c < 4; ++c) mbar_init(bar(B_VFREE + c), 1);
     mbar_init(bar(B_OFULL), 1);
     mbar_init(bar(B_SYNCA), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCB), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCC), SOFTMAX_WARPS);
-    mbar_init(bar(B_FINAL), 1);
+    mbar_init(bar(B_FINQ), 1);
+    mbar_init(bar(B_FINP), 1);
     fence_mbarrier_init();
   }
   if (tid < H) {
@@ -328,15 +335,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t kv_base = smem_u32(kv_s), q_base = smem_u32(q_s);
   bool ok = true;
 
   if (warp >= SOFTMAX_WARP0) {
-    // ---------------- softmax warps (warp 8 also issues the MMAs) ----------------
+    // ---------------- softmax warps (warp 8 also issues the P V MMAs) ----------------
     const int q4 = warp & 3;                        // TMEM lane quadrant
     const int half = (warp - SOFTMAX_WARP0) >> 2;  // heads [32 half, 32 half + 32)
     const int sw = warp - SOFTMAX_WARP0;            // softmax warp 0..7
     const bool issuer = (warp == SOFTMAX_WARP0);
-    const int j = 32 * q4 + lane;                   // KV row of the tile = TMEM lane
+    const bool row_lane = lane < 16;                // lanes 16..31 hold no row of an M = 64 accumulator
+    const int j = 16 * q4 + (lane & 15);            // KV row of the tile held by this lane
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
     const float qk_scale = a.softmax_scale * LOG2E;
     // P' = p s_j 2^E with p <= 256: pick E so that 256 * max_j s_j * 2^E <= 2^15
@@ -350,77 +359,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       }
     }
     const float p_scale = ldexpf(1.f, p_exp);
-    unsigned char* p_row = kv_s + 8 * KATOM_BYTES;
-    const uint32_t kv_base = smem_u32(kv_s), q_base = smem_u32(q_s);
-    const uint32_t p_base = kv_base + 8 * KATOM_BYTES;
-    constexpr uint32_t ID_QK = idesc_f16_f32(128, 64, 0, 0, 0);
     constexpr uint32_t ID_PV = idesc_f16_f32(128, 64, 1, 1, 0);
 
-    // S^T = K Q^T for tile lt, slice pair by slice pair as the gather warps
-    // fill them.  The 16-wide steps alternate between 2 accumulators:
-    // part = step & 1.
-    auto issue_qk = [&](int lt) -> bool {
-      for (int c = 0; c < 5; ++c) {
-        if (!mbar_wait(bar(B_KV + c), lt & 1)) return false;
-        tc_fence_after_sync();
-        const int nsl = c < 4 ? 2 : 1;
+    // O^T += V^T P^T for the tile in buffer b: the 4 independent 128-dim
+    // chunks are issued round robin so that consecutive MMAs never share an
+    // accumulator
+    auto issue_pv = [&](int lt, int b) {
+      const uint64_t a0 = smem_desc_sw128(kv_base + b * TILE_BYTES, KATOM_BYTES, 1024);
+      const uint64_t b0 = smem_desc_sw128(kv_base + b * TILE_BYTES + 8 * KATOM_BYTES, KATOM_BYTES, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          for (int u = 0; u < nsl; ++u) {
-            const int ka = 2 * c + u;
-            const uint32_t part = kk & 1;
-            const uint64_t ad = smem_desc_sw128(kv_base + ka * KATOM_BYTES + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(q_base + ka * QATOM_BYTES + kk * 32, 16, 1024);
-            mma_f16_ss(tmem + TM_S + 64 * part, ad, bd, ID_QK, (c > 0 || u > 0 || kk > 1) ? 1u : 0u);
-          }
-        }
-      }
-      mma_commit(bar(B_SFULL));
-      return true;
-    };
-    // O^T += V^T P^T for tile lt: the 4 independent 128-dim chunks are issued
-    // round robin so that consecutive MMAs never share an accumulator
-    auto issue_pv = [&](int lt) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < T / 16; ++kk) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint64_t ad = smem_desc_sw128(kv_base + 2 * c * KATOM_BYTES + kk * 2048, KATOM_BYTES, 1024);
-          const uint64_t bd = smem_desc_sw128(p_base + kk * 2048, KATOM_BYTES, 1024);
-          mma_f16_ss(tmem + TM_O + 64 * c, ad, bd, ID_PV, (lt > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ss_warp(tmem + TM_O + 64 * c, a0 + ((2 * c * KATOM_BYTES + kk * 2048) >> 4), b0 + ((kk * 2048) >> 4),
+                          ID_PV, (lt > 0 || kk > 0) ? 1u : 0u);
         }
       }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) mma_commit(bar(B_VFREE + c));
+      mma_commit_warp(bar(B_BFREE + b));
     };
-
-    if (issuer) {
-      if (lane == 0) {
-        if (!mbar_wait(bar(B_QFULL), 0) || !issue_qk(0)) ok = false;
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-    }
 
     float l_part[32];
 #pragma unroll
     for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
     uint32_t ph_a = 0, ph_b = 0, ph_c = 0;  // completed phases of the group barriers
-    auto group_sync = [&](int b, uint32_t& ph) {
+    auto group_sync = [&](int bb, uint32_t& ph) {
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(b));
-      const bool done = mbar_wait(bar(b), ph & 1);
+      if (lane == 0) mbar_arrive(bar(bb));
+      const bool done = wait_warp(bb, ph & 1);
       ++ph;
       return done;
     };
     // (slot, scale) of this thread's row, one tile ahead
     auto row_info = [&](int lt) -> int2 {
       const int e = (t_begin + lt) * T + j;
-      return e < a.k ? __ldg(row_res + e) : make_int2(-1, 0);
+      return (row_lane && e < a.k) ? __ldg(row_res + e) : make_int2(-1, 0);
     };
     int2 info = row_info(0);
     for (int lt = 0; lt < ntl && ok; ++lt) {
+      const int b = lt & 1;
       const int2 info_next = lt + 1 < ntl ? row_info(lt + 1) : make_int2(-1, 0);
-      if (!mbar_wait(bar(B_SFULL), lt & 1)) {
+      if (!wait_warp(B_SFULL + b, (lt >> 1) & 1)) {
         ok = false;
         break;
       }
@@ -428,13 +406,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       const bool valid = info.x >= 0;
       const float sc = __int_as_float(info.y);
       const float cj = sc * qk_scale;
-      // logits of row j in the log2 domain (invalid rows: -inf)
+      // logits of row j in the log2 domain (invalid rows and idle lanes: -inf)
       auto load_z = [&](float (&z)[32]) {
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           float v0[16], v1[16];
-          tmem_ld16(t_lane + TM_S + half * 32 + 16 * g, v0);
-          tmem_ld16(t_lane + TM_S + 64 + half * 32 + 16 * g, v1);
+          tmem_ld16(t_lane + TM_S + 64 * (2 * b) + half * 32 + 16 * g, v0);
+          tmem_ld16(t_lane + TM_S + 64 * (2 * b + 1) + half * 32 + 16 * g, v1);
           tmem_wait_ld();
 #pragma unroll
           for (int h = 0; h < 16; ++h) z[16 * g + h] = valid ? (v0[h] + v1[h]) * cj : -INFINITY;
@@ -444,8 +422,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       load_z(z);
       // Fast path: probabilities are taken against the heads' current
       // reference maxima; that stays exact as long as no logit exceeds its
-      // reference by more than 2^EXCEED (no overflow anywhere).  One vote
-      // of the 8 warps decides; only then is the tile maximum reduced.
+      // reference by more than 2^EXCEED (p <= 256, no fp16 overflow).  One
+      // vote of the 8 warps decides; only then is the tile maximum reduced.
       bool bad = false;
       {
         const float4* mu4 = reinterpret_cast<const float4*>(muse_s + half * 32);
@@ -492,6 +470,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
           break;
         }
         if (resc_s[half]) {
+          // O must hold every P V issued so far: the previous tile's
+          if (!wait_warp(B_BFREE + (b ^ 1), ((lt - 1) >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
           const float* al = alpha_s + half * 32;
 #pragma unroll
           for (int h = 0; h < 32; ++h) l_part[h] *= al[h];
@@ -513,7 +497,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
         load_z(z);  // S is still in TMEM: reload rather than keep z live across the rescale
       }
       // probabilities, folded with the row's dequantisation scale and the
-      // query's power of two, as fp16 P
+      // query's power of two, as fp16 P (row j of the rope slice of buffer b)
       uint32_t pk[16];
       const float sp = sc * p_scale;
       const float4* mu4 = reinterpret_cast<const float4*>(muse_s + half * 32);
@@ -528,42 +512,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
           const float p1 = valid ? ex2(z[h + 1] - mm[2 * t + 1]) : 0.f;
           l_part[h] += p0;
           l_part[h + 1] += p1;
-          const __half2 b = __floats2half2_rn(p0 * sp, p1 * sp);
-          pk[h / 2] = *reinterpret_cast<const uint32_t*>(&b);
+          const __half2 hp = __floats2half2_rn(p0 * sp, p1 * sp);
+          pk[h / 2] = *reinterpret_cast<const uint32_t*>(&hp);
         }
       }
+      if (row_lane) {
+        unsigned char* p_row = kv_s + b * TILE_BYTES + 8 * KATOM_BYTES;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        *reinterpret_cast<uint4*>(p_row + sw128(j, half * 4 + cc)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        for (int cc = 0; cc < 4; ++cc) {
+          *reinterpret_cast<uint4*>(p_row + sw128(j, half * 4 + cc)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL));
       if (issuer) {
-        if (lane == 0) {
-          if (!mbar_wait(bar(B_PFULL), lt & 1)) {
-            ok = false;
-          } else {
-            tc_fence_after_sync();
-            issue_pv(lt);
-            if (lt + 1 < ntl && !issue_qk(lt + 1)) ok = false;
-          }
+        ok = wait_warp(B_PFULL, lt & 1);
+        if (ok) {
+          tc_fence_after_sync();
+          issue_pv(lt, b);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       info = info_next;
     }
     if (issuer) {
-      if (lane == 0) {
-        mma_commit(bar(B_OFULL));
-        mma_commit(bar(B_FINAL));
-      }
       __syncwarp();
+      mma_commit_warp(bar(B_OFULL));
+      mma_commit_warp(bar(B_FINP));
     }
     // ---------------- epilogue: normalise and write ----------------
-    if (ok && !mbar_wait(bar(B_OFULL), 0)) ok = false;
+    if (ok && !wait_warp(B_OFULL, 0)) ok = false;
     if (ok) {
       tc_fence_after_sync();
       red_s[q4 * H + half * 32 + lane] = warp_transpose_reduce<false>(l_part, lane);
@@ -610,27 +590,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       report(a.dev_status, DSA_DEV_TIMEOUT);
     }
     // all issued MMAs must be finished before TMEM is released
-    if (issuer && lane == 0 && !mbar_wait(bar(B_FINAL), 0)) report(a.dev_status, DSA_DEV_TIMEOUT);
+    if (issuer && lane == 0 && !mbar_wait(bar(B_FINP), 0)) report(a.dev_status, DSA_DEV_TIMEOUT);
     __syncwarp();
   } else {
-    // ---------------- gather warps: FP8 rows -> registers -> fp16 swizzled tile ----------------
+    // ---------------- gather warps: FP8 rows -> registers -> fp16 swizzled tiles ----------------
     const int gtid = warp * 32 + lane;  // 0..255
-    // rows of the tile this thread gathers: 4 for the slice pairs, 2 for the rope slice
+    const bool qk_issuer = (warp == 0);
+    constexpr uint32_t ID_QK = idesc_f16_f32(64, 64, 0, 0, 0);
+    // S^T = K Q^T for the tile in buffer b; the 16-wide steps alternate
+    // between the 2 partial accumulators of that buffer
+    auto issue_qk = [&](int b) {
+      const uint64_t a0 = smem_desc_sw128(kv_base + b * TILE_BYTES, 16, 1024);
+      const uint64_t b0 = smem_desc_sw128(q_base, 16, 1024);
+#pragma unroll
+      for (int ka = 0; ka < NKA; ++ka) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t part = kk & 1;
+          mma_f16_ss_warp(tmem + TM_S + 64 * (2 * b + part), a0 + ((ka * KATOM_BYTES + kk * 32) >> 4),
+                          b0 + ((ka * QATOM_BYTES + kk * 32) >> 4), ID_QK, (ka > 0 || kk > 1) ? 1u : 0u);
+        }
+      }
+      mma_commit_warp(bar(B_SFULL + b));
+    };
+    // rows of the tile this thread gathers: 2 for the slice pairs, 1 for the rope slice
     int pr_row[PAIR_CHUNKS], rp_row[ROPE_CHUNKS];
 #pragma unroll
     for (int u = 0; u < PAIR_CHUNKS; ++u) pr_row[u] = (gtid + GATHER_THREADS * u) >> 3;
 #pragma unroll
     for (int u = 0; u < ROPE_CHUNKS; ++u) rp_row[u] = (gtid + GATHER_THREADS * u) >> 2;
-    auto load_slots = [&](int lt, int (&ps)[PAIR_CHUNKS], int (&rs)[ROPE_CHUNKS]) {
-      const int base = (t_begin + lt) * T;
-#pragma unroll
-      for (int u = 0; u < PAIR_CHUNKS; ++u) ps[u] = base + pr_row[u] < a.k ? __ldg(&row_res[base + pr_row[u]].x) : -1;
-#pragma unroll
-      for (int u = 0; u < ROPE_CHUNKS; ++u) rs[u] = base + rp_row[u] < a.k ? __ldg(&row_res[base + rp_row[u]].x) : -1;
-    };
-    int ps[PAIR_CHUNKS], rs[ROPE_CHUNKS];
-    load_slots(0, ps, rs);
-    // Q of this token -> swizzled K-major slices
+    // Q of this token -> swizzled K-major slices (fp16)
     {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK);
       constexpr int CH = DQK / 8;
@@ -647,92 +636,93 @@ __global__ void __launch_bounds__(NTHREADS, 1) mla_tc_kernel(const MlaArgs a, co
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_QFULL));
     }
-    // The next tile's rows, held in registers: for each pair c of 64-column
-    // slices, 4 chunks of 16 bytes (8 lanes per 128-byte row segment), and 2
-    // chunks of the rope slice.
-    uint4 pr[4][PAIR_CHUNKS];
-    uint4 rp[ROPE_CHUNKS];
-    auto load_tile = [&]() {
+    // Two tiles' rows held in registers (stage s holds the tile for buffer s):
+    // for each pair c of 64-column slices 2 chunks of 16 bytes (8 lanes per
+    // 128-byte row segment), and 1 chunk of the rope slice.
+    uint4 pr[2][4][PAIR_CHUNKS];
+    uint4 rp[2][ROPE_CHUNKS];
+    auto load_tile = [&](int lt, uint4 (&prs)[4][PAIR_CHUNKS], uint4 (&rps)[ROPE_CHUNKS]) {
+      const int base = (t_begin + lt) * T;
+      int ps[PAIR_CHUNKS], rs[ROPE_CHUNKS];
+#pragma unroll
+      for (int u = 0; u < PAIR_CHUNKS; ++u) ps[u] = base + pr_row[u] < a.k ? __ldg(&row_res[base + pr_row[u]].x) : -1;
+#pragma unroll
+      for (int u = 0; u < ROPE_CHUNKS; ++u) rs[u] = base + rp_row[u] < a.k ? __ldg(&row_res[base + rp_row[u]].x) : -1;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int u = 0; u < PAIR_CHUNKS; ++u) {
           const int c8 = (gtid + GATHER_THREADS * u) & 7;
-          pr[c][u] = make_uint4(0u, 0u, 0u, 0u);
-          if (ps[u] >= 0) pr[c][u] = ldg_nc(a.kv + (int64_t)ps[u] * DQK + c * 128 + c8 * 16);
+          prs[c][u] = make_uint4(0u, 0u, 0u, 0u);
+          if (ps[u] >= 0) prs[c][u] = ldg_nc(a.kv + (int64_t)ps[u] * DQK + c * 128 + c8 * 16);
         }
       }
 #pragma unroll
       for (int u = 0; u < ROPE_CHUNKS; ++u) {
         const int c16 = (gtid + GATHER_THREADS * u) & 3;
-        rp[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (rs[u] >= 0) rp[u] = ldg_nc(a.kv + (int64_t)rs[u] * DQK + DL + c16 * 16);
+        rps[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (rs[u] >= 0) rps[u] = ldg_nc(a.kv + (int64_t)rs[u] * DQK + DL + c16 * 16);
       }
     };
-    load_tile();
-    if (ntl > 1) load_slots(1, ps, rs);
-    for (int lt = 0; lt < ntl && ok; ++lt) {
+    auto store_tile = [&](int b, const uint4 (&prs)[4][PAIR_CHUNKS], const uint4 (&rps)[ROPE_CHUNKS]) {
+      unsigned char* tile = kv_s + b * TILE_BYTES;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        // slices 2c, 2c+1 are free once PV chunk c of the previous tile is done
-        if (lt > 0 && !mbar_wait(bar(B_VFREE + c), (lt - 1) & 1)) ok = false;
-        if (ok) {
 #pragma unroll
-          for (int u = 0; u < PAIR_CHUNKS; ++u) {
-            const int e = gtid + GATHER_THREADS * u;
-            const int row = e >> 3, c8 = e & 7;
-            const int slice = 2 * c + (c8 >> 2), c16 = c8 & 3;
-            uint4 lo, hi;
-            convert16(pr[c][u], lo, hi);
-            unsigned char* dst = kv_s + slice * KATOM_BYTES;
-            // Each quarter warp (8 lanes: one row, two slices) must hit 8
-            // distinct 16-byte bank groups: lanes of the second slice store
-            // their odd chunk first.
-            const bool odd_first = c8 & 4;
-            *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + (odd_first ? 1 : 0))) = odd_first ? hi : lo;
-            *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + (odd_first ? 0 : 1))) = odd_first ? lo : hi;
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_KV + c));
-      }
-      // slice 8 (rope; it also holds P) is free once the whole previous PV is
-      // done, which the wait on chunk 3 above already covered
-      if (ok) {
-#pragma unroll
-        for (int u = 0; u < ROPE_CHUNKS; ++u) {
+        for (int u = 0; u < PAIR_CHUNKS; ++u) {
           const int e = gtid + GATHER_THREADS * u;
-          const int row = e >> 2, c16 = e & 3;
+          const int row = e >> 3, c8 = e & 7;
+          const int slice = 2 * c + (c8 >> 2), c16 = c8 & 3;
           uint4 lo, hi;
-          convert16(rp[u], lo, hi);
-          unsigned char* dst = kv_s + 8 * KATOM_BYTES;
-          *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16)) = lo;
-          *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + 1)) = hi;
+          convert16(prs[c][u], lo, hi);
+          unsigned char* dst = tile + slice * KATOM_BYTES;
+          // Each quarter warp (8 lanes: one row, two slices) must hit 8
+          // distinct 16-byte bank groups: lanes of the second slice store
+          // their odd chunk first.
+          const bool odd_first = c8 & 4;
+          *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + (odd_first ? 1 : 0))) = odd_first ? hi : lo;
+          *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + (odd_first ? 0 : 1))) = odd_first ? lo : hi;
         }
       }
+#pragma unroll
+      for (int u = 0; u < ROPE_CHUNKS; ++u) {
+        const int e = gtid + GATHER_THREADS * u;
+        const int row = e >> 2, c16 = e & 3;
+        uint4 lo, hi;
+        convert16(rps[u], lo, hi);
+        unsigned char* dst = tile + 8 * KATOM_BYTES;
+        *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16)) = lo;
+        *reinterpret_cast<uint4*>(dst + sw128(row, 2 * c16 + 1)) = hi;
+      }
+    };
+    // one step of the pipeline for the tile lt held in stage `st`
+    auto step = [&](int lt, uint4 (&prs)[4][PAIR_CHUNKS], uint4 (&rps)[ROPE_CHUNKS]) {
+      const int b = lt & 1;
+      // the buffer is free once P V of the tile two back is done
+      if (lt >= 2 && !wait_warp(B_BFREE + b, ((lt - 2) >> 1) & 1)) ok = false;
+      if (ok) store_tile(b, prs, rps);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_KV + 4));
-      if (lt + 1 < ntl) {
-        load_tile();                                // tile lt+1: data in flight during tile lt's MMAs
-        if (lt + 2 < ntl) {
-          load_slots(lt + 2, ps, rs);               // the slots of the tile after it,
-          // and its rows pulled into L2 (one 128-byte line per 8 lanes)
-          if ((gtid & 7) == 0) {
-#pragma unroll
-            for (int u = 0; u < PAIR_CHUNKS; ++u)
-              if (ps[u] >= 0)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) prefetch_line_l2(a.kv + (int64_t)ps[u] * DQK + c * 128);
-          }
-          if ((gtid & 3) == 0) {
-#pragma unroll
-            for (int u = 0; u < ROPE_CHUNKS; ++u)
-              if (rs[u] >= 0) prefetch_line_l2(a.kv + (int64_t)rs[u] * DQK + DL);
-          }
+      if (lane == 0) mbar_arrive(bar(B_KV + b));
+      if (qk_issuer && ok) {
+        ok = (lt > 0 || wait_warp(B_QFULL, 0)) && wait_warp(B_KV + b, (lt >> 1) & 1);
+        if (ok) {
+          tc_fence_after_sync();
+          issue_qk(b);
         }
       }
+      if (ok && lt + 2 < ntl) load_tile(lt + 2, prs, rps);  // two tiles ahead
+    };
+    load_tile(0, pr[0], rp[0]);
+    if (ntl > 1) load_tile(1, pr[1], rp[1]);
+    for (int lt = 0; lt < ntl && ok; lt += 2) {
+      step(lt, pr[0], rp[0]);
+      if (lt + 1 < ntl && ok) step(lt + 1, pr[1], rp[1]);
+    }
+    if (qk_issuer) {
+      __syncwarp();
+      mma_commit_warp(bar(B_FINQ));
+      if (!mbar_wait(bar(B_FINQ), 0) && lane == 0) report(a.dev_status, DSA_DEV_TIMEOUT);
     }
     if (!ok) report(a.dev_status, DSA_DEV_TIMEOUT);
   }

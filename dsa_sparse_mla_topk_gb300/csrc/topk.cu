@@ -34,7 +34,8 @@ namespace {
 constexpr int NT = 512;           // threads per CTA (two CTAs fit on an SM)
 constexpr int HBINS = 4096;       // histogram bins (12 key bits)
 constexpr int MCAP = 6144;        // candidates CTA 0 can hold for the final selection
-constexpr int SAMPLE_SHIFT = 7;   // sample the first 8 of every 128 positions (1/16)
+constexpr int SAMPLE_BLOCK = 128; // the sample takes the first SAMPLE_RUN of every
+constexpr int SAMPLE_RUN = 8;     // SAMPLE_BLOCK positions (1/16)
 
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -209,7 +210,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int64_t row = blockIdx.x / C;
   int32_t* out = idx + row * (int64_t)k;
   const int64_t p = q_pos[row];
@@ -239,12 +240,12 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
   if (tid == 0) vars[1] = vars[2] = 0;
   __syncthreads();
   uint32_t nsampled = 0;
-  for (int64_t blk = lo + (int64_t)tid * 128; blk < hi; blk += (int64_t)NT * 128) {
-    float v[8];  // all 8 loads in flight before the first atomic
+  for (int64_t blk = lo + (int64_t)tid * SAMPLE_BLOCK; blk < hi; blk += (int64_t)NT * SAMPLE_BLOCK) {
+    float v[SAMPLE_RUN];  // all loads in flight before the first atomic
 #pragma unroll
-    for (int t = 0; t < 8; ++t) v[t] = blk + t < hi ? __ldg(s + blk + t) : 0.f;
+    for (int t = 0; t < SAMPLE_RUN; ++t) v[t] = blk + t < hi ? __ldg(s + blk + t) : 0.f;
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
+    for (int t = 0; t < SAMPLE_RUN; ++t) {
       if (blk + t < hi) {
         atomicAdd(&hist[score_key(v[t]) >> 20], 1u);
         ++nsampled;

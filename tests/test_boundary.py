@@ -59,7 +59,7 @@ def test_split_rule(lib):
     """Splits only when query tokens alone leave SMs idle and splitting
     shortens the launch; never more splits than KV tiles."""
     tile = dsa.kv_tile_size(64, 512, 64)
-    assert tile == 128 and dsa.kv_tile_size(16, 64, 16) == 32 and dsa.kv_tile_size(32, 512, 64) == -1
+    assert tile == 64 and dsa.kv_tile_size(16, 64, 16) == 32 and dsa.kv_tile_size(32, 512, 64) == -1
     ntiles = dsa.kv_tile_count(2048, tile)
     assert dsa.pick_num_splits(32768, 64, 512, 64, 2048, num_sms=152) == 1
     assert dsa.pick_num_splits(1024, 64, 512, 64, 2048, num_sms=152) == 1
