@@ -53,6 +53,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   return true;
 }
 
+// Arrive once and add `bytes` to the transaction count the current phase
+// waits for (TMA copies complete_tx against it).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// ---- TMA ----------------------------------------------------------------------
+
+// Four rows (row coordinates r.x .. r.w, any order, out-of-range rows read as
+// zeros) of a 2-D tensor, `x` the first column, into consecutive box rows at
+// `dst`, swizzled as the tensor map says; completes bytes on `bar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int4 r, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(r.x), "r"(r.y), "r"(r.z), "r"(r.w), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_map(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 // ---- fences -------------------------------------------------------------------
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
@@ -109,6 +131,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       : "memory");
 }
 
+// 16 lanes x 32 bits, twice (shape 16x32bx2): threads 0-15 read lanes
+// base + t at columns [col, col + 16), threads 16-31 read lanes base + t - 16
+// at columns [col + SPLIT, col + SPLIT + 16).  This is the natural view of an
+// M = 64 accumulator, whose row r sits in lane 32 (r / 16) + r % 16.
+template <int SPLIT>
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr), "n"(SPLIT));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -116,18 +154,26 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all in 16-byte units), fixed version bits 0b001 at
-// [46,49), swizzle mode at [61,64): 2 = 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+// [46,49), swizzle mode at [61,64): 2 = 128-byte swizzle, 4 = 64-byte.
+// Adding (bytes >> 4) to a descriptor moves its start address, as long as
+// the address stays below 256 KB.
+constexpr uint32_t SWIZZLE_128B = 2, SWIZZLE_64B = 4;
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t swizzle) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
   d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
+  d |= (uint64_t)swizzle << 61;
   return d;
 }
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return smem_desc(saddr, lbo_bytes, sbo_bytes, SWIZZLE_128B);
+}
 
-// Instruction descriptor of kind::f16: A and B both bf16 (ab_bf16 = 1) or
+// Instruction descriptor of kind::f16 (and of kind::f8f6f4, where format 0
+// means E4M3 for A and B): A and B both bf16 (ab_bf16 = 1) or
 // both fp16 (0), fp32 D, shape M x N, A/B major-ness (0 = K-major, 1 =
 // MN-major).
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major, int ab_bf16) {
@@ -167,6 +213,17 @@ __device__ __forceinline__ void mma_f16_ss_warp(uint32_t d_tmem, uint64_t a_desc
 // operations of this thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// kind::f8f6f4 MMA (K = 32 per instruction for 8-bit operands), issued by a
+// converged warp like mma_f16_ss_warp.
+__device__ __forceinline__ void mma_f8_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // tcgen05.commit from the lane that mma_f16_ss_warp elects (whole warp converged).
