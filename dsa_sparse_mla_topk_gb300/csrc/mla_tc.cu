@@ -104,7 +104,10 @@ constexpr int B_SYNCA = B_OF + 1;         // softmax-group sync points
 constexpr int B_SYNCB = B_SYNCA + 1;
 constexpr int B_SYNCC = B_SYNCB + 1;
 constexpr int B_FIN = B_SYNCC + 1;        // every MMA is done (teardown)
-constexpr int NBAR = B_FIN + 1;
+constexpr int B_QREADY = B_FIN + 1;       // Q hi/lo is in shared memory (and stages 1, 2 are free)
+constexpr int B_QLOAD = B_QREADY + 1;     // raw bf16 Q has landed in stages 1, 2
+constexpr int NBAR = B_QLOAD + 1;
+static_assert(2 * STAGE_BYTES == H * DQK * 2, "bf16 Q is staged in KV stages 1 and 2");
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_TMEM + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
@@ -117,23 +120,21 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// two floats -> two E4M3 (round to nearest, saturating), x0 in the low byte
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float x0, float x1) {
-  unsigned short r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
-  return r;
+// f16x2 -> hi = E4M3(x) and lo = E4M3(x - hi) as byte pairs (low half ->
+// low byte).  x - hi is exact in fp16: hi is x rounded to 4 significant bits.
+__device__ __forceinline__ void split_e4m3x2(uint32_t h2, uint32_t& hi, uint32_t& lo) {
+  unsigned short a, b;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(a) : "r"(h2));
+  uint32_t back;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(a));
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h2), *reinterpret_cast<const __half2*>(&back));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(b) : "r"(*reinterpret_cast<const uint32_t*>(&r)));
+  hi = a;
+  lo = b;
 }
-// two E4M3 (low byte first) -> two floats, exactly
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
-}
-// (x0, x1) -> hi = E4M3(x), lo = E4M3(x - hi), as two byte pairs
-__device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = f32x2_to_e4m3x2(x0, x1);
-  const float2 back = e4m3x2_to_f32x2(hi);
-  lo = f32x2_to_e4m3x2(x0 - back.x, x1 - back.y);
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float x0, float x1) {
+  const __half2 h = __floats2half2_rn(x0, x1);  // x0 in the low half
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Per-half-warp transpose-reduction: v[16] per lane (16 heads) -> lane l
@@ -184,6 +185,13 @@ __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __r
   // block (x, y): entries [256 x, 256 x + 256) of query y
   const int64_t i = blockIdx.y;
   const int j = blockIdx.x * 256 + threadIdx.x;
+  // block 0 of each query also pulls the query's Q (72 KB) into L2 for the
+  // attention kernel's bulk copy
+  if (blockIdx.x == 0) {
+    const char* qb = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(a.q) + i * H * DQK);
+    for (int off = threadIdx.x * 128; off < H * DQK * 2; off += 256 * 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + off));
+  }
   float smax = 0.f;
   if (j < a.k) {
     const int64_t e = i * a.k + j;
@@ -293,6 +301,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(bar(B_SYNCB), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCC), SOFTMAX_WARPS);
     mbar_init(bar(B_FIN), 1);
+    mbar_init(bar(B_QREADY), NTMA + SOFTMAX_WARPS);
+    mbar_init(bar(B_QLOAD), 1);
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -304,44 +314,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     alpha_s[tid] = 1.f;
   }
 
-  // Q of this token: bf16 [64 heads][576] -> x 2^qexp -> E4M3 hi (B rows
-  // 0..63) and lo (B rows 64..127), K-major, in the MMA's swizzled layouts
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK);
-    constexpr int CH = DQK / 8;                   // 8-element chunks per head
-    constexpr int PER = H * CH / NTHREADS;        // 9 per thread
-    static_assert(PER * NTHREADS == H * CH, "even split of Q");
-    uint4 qv[PER];
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t kv_base = smem_u32(smem + OFF_KV), q_base = smem_u32(q_s), p_base = smem_u32(p_s);
+  bool ok = true;
+
+  // Q of this token: bf16 [64 heads][576] (bulk-copied into KV stages 1
+  // and 2) -> x 2^qexp -> E4M3 hi (B rows 0..63) and lo (B rows 64..127),
+  // K-major, in the MMA's swizzled layouts.  Done by the TMA warps (once the
+  // copies of tile 0 are out) and the softmax warps together: qt numbers
+  // their NQ threads; named barrier 1 syncs them.
+  constexpr int NQ = (NTMA + SOFTMAX_WARPS) * 32;
+  auto convert_q = [&](int qt) {
+    constexpr int CH = DQK / 8;  // 16-byte chunks (8 bf16) per head
+    const uint4* qraw = reinterpret_cast<const uint4*>(smem + OFF_KV + STAGE_BYTES);
+    auto bf_lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+    auto bf_hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
+    if (!wait_warp(B_QLOAD, 0)) ok = false;
     float mx = 0.f;
+#pragma unroll 4
+    for (int e = qt; e < H * CH; e += NQ) {
+      const uint4 v = qraw[e];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      qv[u] = __ldg(src + tid + NTHREADS * u);
-      const uint32_t w[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[t] << 16)), fabsf(__uint_as_float(w[t] & 0xffff0000u))));
+      for (int t = 0; t < 4; ++t) mx = fmaxf(mx, fmaxf(fabsf(bf_lo(w[t])), fabsf(bf_hi(w[t]))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red_s[warp] = mx;
-    __syncthreads();
-    if (tid == 0) {
+    if (lane == 0) red_s[qt >> 5] = mx;
+    named_barrier_sync(1, NQ);
+    if (qt == 0) {
       float m = red_s[0];
-      for (int w = 1; w < NTHREADS / 32; ++w) m = fmaxf(m, red_s[w]);
+      for (int w = 1; w < NQ / 32; ++w) m = fmaxf(m, red_s[w]);
       int e = 0;
       if (m > 0.f && m <= 3.0e38f) frexpf(m, &e);  // m < 2^e
       *qexp_s = (m > 0.f && m <= 3.0e38f) ? 8 - e : 0;
     }
-    __syncthreads();
+    named_barrier_sync(1, NQ);
     const float qs = ldexpf(1.f, *qexp_s);
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int e = tid + NTHREADS * u;
+#pragma unroll 4
+    for (int e = qt; e < H * CH; e += NQ) {
       const int h = e / CH, c = e % CH;
-      const uint32_t w[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+      const uint4 v = qraw[e];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
-        split_e4m3x2(__uint_as_float(w[t] << 16) * qs, __uint_as_float(w[t] & 0xffff0000u) * qs, hi[t], lo[t]);
+      for (int t = 0; t < 4; ++t) split_e4m3x2(f32x2_to_f16x2(bf_lo(w[t]) * qs, bf_hi(w[t]) * qs), hi[t], lo[t]);
       const uint2 hv = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
       const uint2 lv = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
       const int b = c * 8;  // byte column
@@ -359,14 +379,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       *reinterpret_cast<uint2*>(q_s + off_hi) = hv;
       *reinterpret_cast<uint2*>(q_s + off_lo) = lv;
     }
+    // the raw Q reads and the hi/lo writes are ordered before the TMA
+    // warps' next copies into stages 1, 2 and before the MMAs
     fence_proxy_async_smem();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t kv_base = smem_u32(smem + OFF_KV), q_base = smem_u32(q_s), p_base = smem_u32(p_s);
-  bool ok = true;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(B_QREADY));
+  };
 
   if (warp < SOFTMAX_WARP0 && warp != WARP_MMA) {
     // ---------------- TMA warps: gather the selected rows, 4 per copy ----------------
@@ -375,9 +393,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int my_groups = (GROUPS - tw + NTMA - 1) / NTMA;
     const int g = tw + NTMA * lane;
     int issued = 0;
+    if (tw == 0 && lane == 0) {  // raw Q into stages 1 and 2, converted by the softmax warps
+      mbar_arrive_expect_tx(bar(B_QLOAD), 2 * STAGE_BYTES);
+      tma_bulk_load(kv_base + STAGE_BYTES, static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK,
+                    2 * STAGE_BYTES, bar(B_QLOAD));
+    }
     for (int lt = 0; lt < ntl; ++lt) {
       const int s = lt % NST;
       if (lt >= NST && !wait_warp(B_KVE + s, ((lt - NST) / NST) & 1)) {
+        ok = false;
+        break;
+      }
+      if (lt == 1 && !wait_warp(B_QREADY, 0)) {  // stages 1 and 2 hold raw Q until then
         ok = false;
         break;
       }
@@ -396,6 +423,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_gather4(dst + ROPE_OFF + g * 256, &tmap_rope, DL, rows, bar(B_KVF + s));
       }
       issued = lt + 1;
+      if (lt == 0) convert_q(tw * 32 + lane);  // join the Q conversion once tile 0's copies are out
     }
     // no copy may land after the CTA is gone: wait for the last ones (normally long complete)
     for (int lt = issued > NST ? issued - NST : 0; lt < issued; ++lt)
@@ -441,7 +469,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mma_commit_warp(bar(B_KVE + s));
       mma_commit_warp(bar(B_PVD + pb));
     };
-    ok = wait_warp(B_KVF, 0);
+    ok = wait_warp(B_QREADY, 0) && wait_warp(B_KVF, 0);
     if (ok) {
       tc_fence_after_sync();
       issue_qk(0);
@@ -477,6 +505,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int hg = 2 * h2 + (lane >> 4);            // this thread's heads: [16 hg, 16 hg + 16)
     const int j = 16 * q4 + (lane & 15);            // this thread's tile row
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
+    convert_q(tid - SOFTMAX_WARP0 * 32 + NTMA * 32);
     const float qk_scale = a.softmax_scale * LOG2E * ldexpf(1.f, -*qexp_s);
     // P' = p s_j 2^E with p <= 16: pick E so that 16 max_j s_j 2^E < 256
     int p_exp = 0;
@@ -625,7 +654,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const float p1 = valid ? ex2(z[h + 1] - mm[2 * t + 1]) : 0.f;
           l_part[h] += p0;
           l_part[h + 1] += p1;
-          split_e4m3x2(p0 * sp, p1 * sp, phi[h / 2], plo[h / 2]);
+          split_e4m3x2(f32x2_to_f16x2(p0 * sp, p1 * sp), phi[h / 2], plo[h / 2]);
         }
       }
       {
