@@ -37,7 +37,11 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # DRAM bytes (read + write) per launch of the attention kernel, from one ncu
 # capture, keyed by the SHA-1 of the kernel source it was taken on.  A stale
 # entry (the kernel changed since) is reported as null.
-TRAFFIC_BY_SOURCE: dict[str, dict] = {}
+TRAFFIC_BY_SOURCE: dict[str, dict] = {
+    # ncu --set full, second launch, decode_64k_prefix99.9: 49.05 MB read + 0.75 MB written
+    # (profiles/mla_tc_kernel_decode_64k_prefix99.9.md)
+    "19f21c5a8d04021fceb350d8121d9b8d937a5870": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49805312},
+}
 
 
 def parse_args():
@@ -415,7 +419,8 @@ def bench_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if src.endswith("mla_tc.cu") else "fp32", "data": "synthetic (seeded; shapes of the GLM-5.3-Flash workloads)",
+            "vs_baseline": None, "dtype": "e4m3" if src.endswith("mla_tc.cu") else "fp32",
+            "data": "synthetic (seeded; shapes of the GLM-5.3-Flash workloads)",
             "config": workload_config(w, S, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
             "roofline": {"kernel": "sparse_mla_fwd", "bound": "hbm", "achieved": achieved_gbs,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
