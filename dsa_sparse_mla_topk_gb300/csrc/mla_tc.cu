@@ -39,7 +39,8 @@
 //    mbarriers; every wait is bounded in time and reports DSA_DEV_TIMEOUT
 //    instead of hanging.
 //  * A small resolve kernel first turns every selected position into its
-//    (slot, scale) pair, fully in parallel, into caller-provided scratch.
+//    (slot, scale) pair, fully in parallel, into caller-provided scratch;
+//    the attention kernel is its programmatic dependent and overlaps it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -178,10 +179,11 @@ __device__ __forceinline__ float half_warp_transpose_reduce(const float (&v)[16]
 // Resolve every selected position into (slot, dequantisation scale) once,
 // fully in parallel, so that the attention kernel's gathers depend on one
 // contiguous load instead of a chain of three: idx -> block table -> scale.
-// Invalid or padding entries get slot -1; bad inputs are reported.  It also
-// records the largest scale each query selects (for the range of P).
-__global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __restrict__ res,
-                                                      unsigned int* __restrict__ max_scale_bits) {
+// Invalid or padding entries get slot -1; bad inputs are reported.  The
+// attention kernel is launched as its programmatic dependent: it starts (Q
+// copy and split) while this runs and waits for it before reading `res`.
+__global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __restrict__ res) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // block (x, y): entries [256 x, 256 x + 256) of query y
   const int64_t i = blockIdx.y;
   const int j = blockIdx.x * 256 + threadIdx.x;
@@ -192,7 +194,6 @@ __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __r
     for (int off = threadIdx.x * 128; off < H * DQK * 2; off += 256 * 128)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + off));
   }
-  float smax = 0.f;
   if (j < a.k) {
     const int64_t e = i * a.k + j;
     const int32_t pos = a.idx[e];
@@ -214,30 +215,16 @@ __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __r
         } else {
           slot = page * a.page_size + pos % a.page_size;
           sc = a.kv_scale[slot];
-          smax = sc;
         }
       }
     }
     res[e] = make_int2(slot, __float_as_int(sc));
   }
-  // the block's largest scale, then one atomic per block; scales are
-  // non-negative, so their bit patterns order like the values
-  __shared__ float wmax[8];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
-  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = smax;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = wmax[0];
-    for (int w = 1; w < 8; ++w) m = fmaxf(m, wmax[w]);
-    if (m > 0.f) atomicMax(max_scale_bits + i, __float_as_uint(m));
-  }
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     mla_tc_kernel(const MlaArgs a, const __grid_constant__ CUtensorMap tmap_lat,
-                  const __grid_constant__ CUtensorMap tmap_rope, const int2* __restrict__ res,
-                  const unsigned int* __restrict__ max_scale_bits) {
+                  const __grid_constant__ CUtensorMap tmap_rope, const int2* __restrict__ res) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* q_s = smem + OFF_Q;
@@ -248,6 +235,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   int* vote_s = reinterpret_cast<int*>(smem + OFF_FLAG);  // [2][8] per-tile votes (double buffered)
   int* resc_s = vote_s + 16;                                // [2] rescale needed, per head half
   int* qexp_s = vote_s + 18;                                // Q's power-of-two scale
+  float* smax_s = reinterpret_cast<float*>(vote_s + 20);   // [8] softmax warps' largest scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
   auto bar = [&](int b) { return smem_u32(bars + b); };
@@ -398,6 +386,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_bulk_load(kv_base + STAGE_BYTES, static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK,
                     2 * STAGE_BYTES, bar(B_QLOAD));
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the resolve kernel's entries are complete
     for (int lt = 0; lt < ntl; ++lt) {
       const int s = lt % NST;
       if (lt >= NST && !wait_warp(B_KVE + s, ((lt - NST) / NST) & 1)) {
@@ -507,10 +496,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
     convert_q(tid - SOFTMAX_WARP0 * 32 + NTMA * 32);
     const float qk_scale = a.softmax_scale * LOG2E * ldexpf(1.f, -*qexp_s);
-    // P' = p s_j 2^E with p <= 16: pick E so that 16 max_j s_j 2^E < 256
+    // P' = p s_j 2^E with p <= 16: pick E so that 16 max_j s_j 2^E < 256,
+    // max_j over the entries of this CTA's tiles
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the resolve kernel's entries are complete
     int p_exp = 0;
     {
-      const float smax = __uint_as_float(max_scale_bits[i]);
+      float sm = 0.f;
+      const int e_end = t_end * T < a.k ? t_end * T : a.k;
+      for (int e = t_begin * T + sw * 32 + lane; e < e_end; e += SOFTMAX_WARPS * 32)
+        sm = fmaxf(sm, __int_as_float(__ldg(&row_res[e].y)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, o));
+      if (lane == 0) smax_s[sw] = sm;
+      named_barrier_sync(2, SOFTMAX_WARPS * 32);
+      float smax = smax_s[0];
+#pragma unroll
+      for (int w = 1; w < SOFTMAX_WARPS; ++w) smax = fmaxf(smax, smax_s[w]);
       if (smax > 0.f) {
         int e2;
         frexpf(smax, &e2);  // smax < 2^e2
@@ -763,8 +764,8 @@ bool make_kv_map(CUtensorMap* map, const MlaArgs& a, uint32_t box_cols, CUtensor
 bool mla_tc_supported(const MlaArgs& a) { return a.heads == H && a.d_latent == DL && a.d_rope == DR; }
 
 size_t mla_tc_workspace_bytes(int32_t num_q, int32_t k) {
-  // resolved (slot, scale) per entry, then the largest scale per query
-  return sizeof(int2) * (size_t)num_q * (size_t)k + sizeof(int2) * (((size_t)num_q + 1) / 2);
+  // the resolved (slot, scale) of every selected entry
+  return sizeof(int2) * (size_t)num_q * (size_t)k;
 }
 
 cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream) {
@@ -773,17 +774,27 @@ cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream
   if (!make_kv_map(&map_lat, a, 128, CU_TENSOR_MAP_SWIZZLE_128B) || !make_kv_map(&map_rope, a, DR, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   int2* res = static_cast<int2*>(workspace);
-  unsigned int* max_bits = reinterpret_cast<unsigned int*>(res + (size_t)a.num_q * a.k);
-  cudaError_t e = cudaMemsetAsync(max_bits, 0, sizeof(unsigned int) * (size_t)a.num_q, stream);
-  if (e != cudaSuccess) return e;
   const dim3 rgrid((a.k + 255) / 256, a.num_q);
-  resolve_kernel<<<rgrid, 256, 0, stream>>>(a, res, max_bits);
-  e = cudaGetLastError();
+  resolve_kernel<<<rgrid, 256, 0, stream>>>(a, res);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_q, a.num_splits);
-  mla_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(a, map_lat, map_rope, res, max_bits);
+  // programmatic dependent launch: the attention CTAs may start while the
+  // resolve kernel runs; they wait for it (griddepcontrol.wait) before
+  // reading its entries
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_q, a.num_splits);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mla_tc_kernel, a, map_lat, map_rope, static_cast<const int2*>(res));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -6,23 +6,23 @@
 // and forbids later allocations (cudaMalloc can synchronise the device and
 // stall every other stream), or a host application that calls this library
 // from a plug-in interface that offers no allocator.  This entry point keeps
-// its scratch -- the resolved (slot, scale) of every selected position plus
-// one scale maximum per query token -- in a fixed array of device memory that
-// is part of the library image, so the call itself allocates nothing.
+// its scratch -- the resolved (slot, scale) of every selected position -- in a
+// fixed array of device memory that is part of the library image, so the
+// call itself allocates nothing.
 //
 // Limits and sharing:
 //  * The array holds kNoallocScratchBytes (24 MiB).  A call needs
 //    dsa_sparse_mla_workspace_size() bytes of it -- 8 bytes per selected
-//    entry plus 4 per query token, e.g. 16 MiB for 1024 query tokens at
-//    top-k 2048; calls that need more are rejected with
+//    entry, e.g. 16 MiB for 1024 query tokens at top-k 2048; calls that need
+//    more are rejected with
 //    DSA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
 //  * Every GPU that loads the library holds its own copy of the array until
 //    the process exits.
 //  * All calls share the array.  Two calls whose work overlaps on the GPU
 //    (different streams without ordering between them, or different host
 //    threads) race on it and may produce wrong results; serialise them.
-//  * The per-query maxima must start at zero on every call; the call clears
-//    them on its stream before use.  The resolved entries are fully rewritten.
+//  * Nothing in the array needs clearing: every call rewrites the entries it
+//    uses before reading them.
 //  * The device address of the array is looked up once per device, with that
 //    device current, on the first call made while it is the current device.
 //    Make that first call before starting any stream capture on the device.

@@ -133,7 +133,7 @@ def test_combine_argument_checks(lib, args, expect):
 
 
 def test_workspace_size(lib):
-    assert dsa.sparse_mla_workspace_size(128, 64, 512, 64, 2048) == 128 * 2048 * 8 + 64 * 8
+    assert dsa.sparse_mla_workspace_size(128, 64, 512, 64, 2048) == 128 * 2048 * 8
     assert dsa.sparse_mla_workspace_size(2, 16, 64, 16, 64) == 0
     assert dsa.sparse_mla_workspace_size(0, 64, 512, 64, 2048) == 0
 
