@@ -179,9 +179,11 @@ __device__ __forceinline__ float half_warp_transpose_reduce(const float (&v)[16]
 // Resolve every selected position into (slot, dequantisation scale) once,
 // fully in parallel, so that the attention kernel's gathers depend on one
 // contiguous load instead of a chain of three: idx -> block table -> scale.
-// Invalid or padding entries get slot -1; bad inputs are reported.  The
-// attention kernel is launched as its programmatic dependent: it starts (Q
-// copy and split) while this runs and waits for it before reading `res`.
+// Invalid or padding entries get slot -1; bad inputs are reported.  It is
+// itself a programmatic dependent of the previous kernel on the stream
+// (normally the top-k, whose indices it reads), and the attention kernel is
+// its programmatic dependent: that starts (Q copy and split) while this runs
+// and waits for it before reading `res`.
 __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __restrict__ res) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // block (x, y): entries [256 x, 256 x + 256) of query y
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __r
     for (int off = threadIdx.x * 128; off < H * DQK * 2; off += 256 * 128)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + off));
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the indices are complete
   if (j < a.k) {
     const int64_t e = i * a.k + j;
     const int32_t pos = a.idx[e];
@@ -774,9 +777,17 @@ cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream
   if (!make_kv_map(&map_lat, a, 128, CU_TENSOR_MAP_SWIZZLE_128B) || !make_kv_map(&map_rope, a, DR, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   int2* res = static_cast<int2*>(workspace);
-  const dim3 rgrid((a.k + 255) / 256, a.num_q);
-  resolve_kernel<<<rgrid, 256, 0, stream>>>(a, res);
-  cudaError_t e = cudaGetLastError();
+  // both launches are programmatic dependents of the kernel before them
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t rcfg = {};
+  rcfg.gridDim = dim3((a.k + 255) / 256, a.num_q);
+  rcfg.blockDim = dim3(256);
+  rcfg.stream = stream;
+  rcfg.attrs = attr;
+  rcfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&rcfg, resolve_kernel, a, res);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -788,9 +799,6 @@ cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, mla_tc_kernel, a, map_lat, map_rope, static_cast<const int2*>(res));

@@ -208,6 +208,9 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
   // vars: [0] T_lo (CTA 0), [1] candidate count, [2] overflow, [3] sampled count
   __shared__ uint32_t vars[4];
 
+  // the next kernel on the stream (the attention call's resolve step) may be
+  // scheduled now; it waits for this grid's results before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int tid = threadIdx.x;
