@@ -52,6 +52,10 @@ def _load():
             lib.oracle_sparse_mla.restype = ctypes.c_int
             lib.oracle_combine.argtypes = [c_p, c_p, c_i32, c_i64, c_i32, c_i32, c_p, c_p]
             lib.oracle_combine.restype = ctypes.c_int
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_kv_write.argtypes = [c_p, c_i64, c_i32, c_p, c_p, c_p, c_i32, c_i32, c_i32, c_i64, c_p, c_p]
+            lib.oracle_kv_write.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -127,3 +131,26 @@ def combine(o_part, lse_part):
     lse = np.empty((num_q, H), dtype=np.float64)
     _load().oracle_combine(_ptr(op), _ptr(lp), S, num_q, H, dv, _ptr(out), _ptr(lse))
     return out, lse
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest FP8 E4M3 code of a finite float32, ties to even, saturating at 448."""
+    return int(_load().oracle_e4m3_encode(float(np.float32(x))))
+
+
+def kv_write(rows_bits, req, pos, block_table, kv, kv_scale, *, page_size):
+    """Quantise bf16 rows ([n, d] bit patterns) to FP8 E4M3 with one fp32 scale
+    per token (scale = max|x| / 448, bytes = e4m3(x / scale), fp32 divisions)
+    and store them, in place, into ``kv`` (uint8 [slots, d]) and ``kv_scale``
+    (fp32 [slots]) at slot = block_table[req][pos // P] * P + pos % P.
+    Returns the status bits (BAD_INDEX, BAD_PAGE) of skipped rows."""
+    x = np.asarray(rows_bits)
+    x = _c(x.view(np.uint16) if x.dtype == np.int16 else x, np.uint16)
+    rq = _c(req, np.int32)
+    ps = _c(pos, np.int32)
+    bt = _c(block_table, np.int32)
+    assert kv.dtype == np.uint8 and kv.flags.c_contiguous and kv_scale.dtype == np.float32
+    assert kv_scale.flags.c_contiguous and kv.shape == (kv_scale.shape[0], x.shape[1])
+    assert kv.shape[0] % page_size == 0
+    return _load().oracle_kv_write(_ptr(x), x.shape[0], x.shape[1], _ptr(rq), _ptr(ps), _ptr(bt), bt.shape[0],
+                                   bt.shape[1], page_size, kv.shape[0] // page_size, _ptr(kv), _ptr(kv_scale))

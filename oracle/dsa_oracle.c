@@ -396,3 +396,78 @@ int oracle_combine(const double* o_part, const double* lse_part, int32_t S, int6
           out + i * (int64_t)H * dv, lse + i * (int64_t)H);
   return ORACLE_OK;
 }
+
+/* ---- KV cache write: per-token FP8 quantisation and paged scatter ------ */
+
+/* Nearest FP8 E4M3 code of a finite float, ties to even, magnitudes at or
+ * above the largest finite value (448) saturating to it (E4M3 has no
+ * infinity).  On the E4M3 grid a normal binade [2^e, 2^(e+1)) has 8 steps of
+ * 2^(e-3); below 2^-6 the subnormal step is 2^-9.  Scaling by a power of two
+ * and rint() (round half to even in the default rounding mode) are exact in
+ * double. */
+uint8_t oracle_e4m3_encode(float y) {
+  const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  const double a = fabs((double)y);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal codes 0..7; rounding up to 8 gives the smallest normal, code 8 */
+    const double m = rint(a / ldexp(1.0, -9));
+    return sign | (uint8_t)m;
+  }
+  int e2;
+  frexp(a, &e2); /* a = f * 2^e2, f in [0.5, 1): a lies in [2^(e2-1), 2^e2) */
+  int e = e2 - 1;
+  double m = rint(a / ldexp(1.0, e - 3)); /* 8..16 */
+  if (m == 16.0) {
+    m = 8.0;
+    e += 1;
+  }
+  /* a < 448 keeps the result at or below 1.75 * 2^8 (code 0x7E) */
+  return sign | (uint8_t)(((e + 7) << 3) | ((int)m - 8));
+}
+
+/* Store n new KV rows.  Row i (bf16 values x, d of them) belongs to request
+ * req[i] at position pos[i]; its slot is block_table[req][pos / P] * P +
+ * pos % P (the paged pool of "KV-only decode RadixCache", LMSYS section 2).
+ * The row is stored as FP8 E4M3 with one fp32 scale per token (SGLang
+ * cookbook, "Keep the KV and DSA backends paired"): amax = max |x|, scale =
+ * amax / 448 and byte_j = e4m3(x_j / scale), both divisions in fp32 as the
+ * device computes them (the quantised codes are decided in that precision).
+ * An all-zero row gets scale 0 and zero bytes.  Rows whose request, position
+ * or page is out of range are skipped and flagged (BAD_INDEX for a position
+ * outside the block table, BAD_PAGE for a request or page id out of range). */
+int oracle_kv_write(const uint16_t* rows, int64_t n, int32_t d, const int32_t* req, const int32_t* pos,
+                    const int32_t* block_table, int32_t num_req, int32_t bt_stride, int32_t page_size,
+                    int64_t num_pages, uint8_t* kv, float* kv_scale) {
+  int status = ORACLE_OK;
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t r = req[i], p = pos[i];
+    if (r < 0 || r >= num_req) {
+      status |= ORACLE_BAD_PAGE;
+      continue;
+    }
+    if (p < 0 || p / page_size >= bt_stride) {
+      status |= ORACLE_BAD_INDEX;
+      continue;
+    }
+    const int32_t page = block_table[(int64_t)r * bt_stride + p / page_size];
+    if (page < 0 || page >= num_pages) {
+      status |= ORACLE_BAD_PAGE;
+      continue;
+    }
+    const int64_t slot = (int64_t)page * page_size + p % page_size;
+    const uint16_t* x = rows + i * (int64_t)d;
+    float amax = 0.0f;
+    for (int32_t j = 0; j < d; ++j) {
+      const float v = fabsf((float)oracle_bf16_to_double(x[j]));
+      if (v > amax) amax = v;
+    }
+    const float scale = amax / 448.0f;
+    kv_scale[slot] = scale;
+    for (int32_t j = 0; j < d; ++j) {
+      const float v = (float)oracle_bf16_to_double(x[j]);
+      kv[slot * d + j] = scale > 0.0f ? oracle_e4m3_encode(v / scale) : 0;
+    }
+  }
+  return status;
+}

@@ -274,3 +274,111 @@ def test_bad_index_and_page_are_reported():
         oracle.sparse_mla(inp.q.view(torch.int16).numpy(), inp.kv.numpy(), inp.kv_scale.numpy(), bt,
                           inp.q_req.numpy(), idx, d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size,
                           softmax_scale=w.scale)
+
+
+# ---- KV cache write path: FP8 E4M3 encoding and paged scatter ----
+
+def _e4m3_grid():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    ok = np.isfinite(vals)
+    return codes[ok], vals[ok]
+
+
+def test_e4m3_encode_matches_torch_on_grid_ties_and_random_values():
+    """The encoder against torch's float8_e4m3fn cast (round to nearest even):
+    every grid value, every midpoint between neighbours (ties), points just off
+    the midpoints, and random values across the whole range."""
+    _, vals = _e4m3_grid()
+    pos = np.unique(vals[vals >= 0]).astype(np.float64)
+    mids = (pos[:-1] + pos[1:]) / 2
+    rng = np.random.default_rng(5)
+    rand = np.concatenate([rng.uniform(-448, 448, 4000), rng.uniform(-2.0 ** -5, 2.0 ** -5, 2000),
+                           np.exp2(rng.uniform(-12, 8.8, 4000)) * rng.choice([-1, 1], 4000)])
+    xs = np.concatenate([pos, -pos, mids, -mids, np.nextafter(mids, 0), np.nextafter(mids, 1000), rand])
+    xs = xs[np.abs(xs) <= 448].astype(np.float32)
+    want = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(x) for x in xs], dtype=np.uint8)
+    # +0.0 and -0.0 both encode to a zero of their own sign in both
+    assert np.array_equal(got, want)
+
+
+def test_e4m3_encode_saturates_and_keeps_sign():
+    assert oracle.e4m3_encode(448.0) == 0x7E and oracle.e4m3_encode(-448.0) == 0xFE
+    assert oracle.e4m3_encode(464.0) == 0x7E and oracle.e4m3_encode(1e30) == 0x7E
+    assert oracle.e4m3_encode(-3.4e38) == 0xFE
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00 and oracle.e4m3_encode(-(2.0 ** -10)) == 0x80
+    assert oracle.e4m3_encode(1.0) == 0x38 and oracle.e4m3_encode(-1.0) == 0xB8
+
+
+def _rows_bf16(n, d, seed, spread=False):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((n, d), generator=g)
+    if spread:  # per-row magnitudes from 2^-20 to 2^20
+        x = x * torch.exp2(torch.randint(-20, 21, (n, 1), generator=g).float())
+    return x.to(torch.bfloat16)
+
+
+def test_kv_write_matches_an_independent_torch_quantiser():
+    """Per-token quantisation (scale = max|x|/448, bytes = RNE(x/scale) on the
+    E4M3 grid) against the input generator's torch implementation, on rows of
+    very different magnitudes; identity block table."""
+    n, d, P = 96, 576, 32
+    x = _rows_bf16(n, d, 11, spread=True)
+    want_b, want_s = wl.quantize_rows(x.float())
+    kv = np.zeros((n, d), dtype=np.uint8)
+    sc = np.zeros(n, dtype=np.float32)
+    bt = np.arange(n // P, dtype=np.int32)[None, :]
+    st = oracle.kv_write(x.view(torch.int16).numpy(), np.zeros(n, np.int32), np.arange(n, dtype=np.int32), bt, kv,
+                         sc, page_size=P)
+    assert st == oracle.OK
+    assert np.array_equal(sc, want_s.numpy())
+    assert np.array_equal(kv, want_b.numpy())
+
+
+def test_kv_write_dequantises_within_half_a_step():
+    """Dequantised values lie within half an E4M3 step (relative 2^-4, or the
+    subnormal step) of the bf16 inputs, and the row maximum is exact."""
+    n, d, P = 16, 80, 16
+    x = _rows_bf16(n, d, 12)
+    kv = np.zeros((n, d), dtype=np.uint8)
+    sc = np.zeros(n, dtype=np.float32)
+    oracle.kv_write(x.view(torch.int16).numpy(), np.zeros(n, np.int32), np.arange(n, dtype=np.int32),
+                    np.arange(1, dtype=np.int32)[None, :], kv, sc, page_size=P)
+    deq = np.array([[oracle.e4m3_to_double(b) for b in row] for row in kv]) * sc[:, None].astype(np.float64)
+    xv = x.double().numpy()
+    step = np.maximum(np.abs(xv) * 2.0 ** -4, sc[:, None] * 2.0 ** -10)
+    assert np.all(np.abs(deq - xv) <= step * (1 + 1e-6))
+    amax_rows = np.argmax(np.abs(xv), axis=1)
+    assert np.allclose(np.abs(deq[np.arange(n), amax_rows]), np.abs(xv[np.arange(n), amax_rows]), rtol=1e-6)
+
+
+def test_kv_write_scatters_through_the_block_table():
+    """Rows land at block_table[req][pos // P] * P + pos % P and nowhere else;
+    a zero row stores scale 0 and zero bytes; bad requests, positions and pages
+    are flagged and skipped."""
+    P, d = 8, 32
+    bt = np.array([[5, 2, 7], [1, 6, 0]], dtype=np.int32)  # 8 pages
+    req = np.array([0, 0, 1, 1, 1, 0, 2, 1], dtype=np.int32)
+    pos = np.array([0, 13, 23, 9, 5, 30, 1, -1], dtype=np.int32)
+    x = _rows_bf16(len(req), d, 13)
+    x[4] = 0
+    kv = np.full((8 * P, d), 0xAA, dtype=np.uint8)
+    sc = np.full(8 * P, -1.0, dtype=np.float32)
+    st = oracle.kv_write(x.view(torch.int16).numpy(), req, pos, bt, kv, sc, page_size=P)
+    assert st == oracle.BAD_INDEX | oracle.BAD_PAGE  # pos 30 past the table and -1; request 2
+    written = {}
+    for i in range(5):
+        slot = int(bt[req[i], pos[i] // P]) * P + int(pos[i]) % P
+        written[slot] = i
+        want_b, want_s = wl.quantize_rows(x[i:i + 1].float())
+        if i == 4:
+            assert sc[slot] == 0.0 and not kv[slot].any()
+        else:
+            assert sc[slot] == want_s.item() and np.array_equal(kv[slot], want_b.numpy()[0])
+    untouched = np.array([s for s in range(8 * P) if s not in written])
+    assert np.all(sc[untouched] == -1.0) and np.all(kv[untouched] == 0xAA)
+    bad_page = np.array([[9]], dtype=np.int32)
+    st = oracle.kv_write(x[:1].view(torch.int16).numpy(), np.zeros(1, np.int32), np.zeros(1, np.int32), bad_page,
+                         kv, sc, page_size=P)
+    assert st == oracle.BAD_PAGE
