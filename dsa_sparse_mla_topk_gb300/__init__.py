@@ -14,7 +14,7 @@ import threading
 
 import torch
 
-__all__ = ["DsaError", "load_library", "topk_select", "sparse_mla_fwd", "combine", "sparse_mla_topk",
+__all__ = ["DsaError", "load_library", "topk_select", "sparse_mla_fwd", "combine", "sparse_mla_topk", "kv_write",
            "kv_tile_count", "kv_tile_size", "pick_num_splits", "status_string", "EXPORTED_SYMBOLS",
            "DEV_BAD_QPOS", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT"]
 
@@ -26,7 +26,7 @@ DEV_BAD_QPOS, DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/dsa.h declares.
 EXPORTED_SYMBOLS = ("dsa_status_string", "dsa_version", "dsa_topk_select", "dsa_topk_workspace_size",
                     "dsa_sparse_mla_fwd", "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_fwd_noalloc",
-                    "dsa_combine", "dsa_kv_tile_count", "dsa_kv_tile_size",
+                    "dsa_combine", "dsa_kv_write", "dsa_kv_tile_count", "dsa_kv_tile_size",
                     "dsa_pick_num_splits")
 
 _lock = threading.Lock()
@@ -70,6 +70,8 @@ def load_library(path: str | None = None):
         lib.dsa_sparse_mla_fwd.restype = i32
         lib.dsa_combine.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         lib.dsa_combine.restype = i32
+        lib.dsa_kv_write.argtypes = [vp, i32, i32, vp, vp, vp, i32, i32, i32, i64, vp, vp, vp, vp]
+        lib.dsa_kv_write.restype = i32
         lib.dsa_kv_tile_count.argtypes = [i32, i32]
         lib.dsa_kv_tile_count.restype = i32
         lib.dsa_kv_tile_size.argtypes = [i32, i32, i32]
@@ -208,6 +210,28 @@ def combine(o_part: torch.Tensor, lse_part: torch.Tensor, out=None, lse=None, st
         lse = torch.empty((num_q, H), dtype=torch.float32, device=o_part.device)
     _call("dsa_combine", _p(o_part), _p(lse_part), S, num_q, H, dv, _p(out), _p(lse), _stream(stream))
     return out, lse
+
+
+def kv_write(rows: torch.Tensor, req: torch.Tensor, pos: torch.Tensor, block_table: torch.Tensor,
+             kv: torch.Tensor, kv_scale: torch.Tensor, *, page_size: int, dev_status=None, stream=None):
+    """Quantise bf16 rows [n, d_qk] to FP8 E4M3 with one fp32 scale per token
+    and store them, in place, into the paged cache ``kv`` (uint8 [slots, d_qk])
+    and ``kv_scale`` (fp32 [slots]) at each row's (request, position) slot."""
+    _check(rows, "rows", torch.bfloat16, 2)
+    _check(req, "req", torch.int32, 1)
+    _check(pos, "pos", torch.int32, 1)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(kv, "kv", torch.uint8, 2)
+    _check(kv_scale, "kv_scale", torch.float32, 1)
+    n, d = rows.shape
+    if req.shape != (n,) or pos.shape != (n,) or kv.shape[1] != d or kv.shape[0] != kv_scale.shape[0]:
+        raise ValueError("inconsistent shapes")
+    if kv.shape[0] % page_size:
+        raise ValueError("kv rows must be a whole number of pages")
+    _call("dsa_kv_write", _p(rows), n, d, _p(req), _p(pos), _p(block_table), block_table.shape[0],
+          block_table.shape[1], page_size, kv.shape[0] // page_size, _p(kv), _p(kv_scale), _p(dev_status),
+          _stream(stream))
+    return kv, kv_scale
 
 
 def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, *, d_latent: int, d_rope: int,

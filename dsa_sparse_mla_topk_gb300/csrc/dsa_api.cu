@@ -174,3 +174,17 @@ dsa_status dsa_combine(const float* o_part, const float* lse_part, int32_t num_s
 }
 
 }  // extern "C"
+
+dsa_status dsa_kv_write(const void* rows, int32_t n, int32_t d_qk, const int32_t* req, const int32_t* pos,
+                        const int32_t* block_table, int32_t num_req, int32_t bt_stride, int32_t page_size,
+                        int64_t num_pages, uint8_t* kv, float* kv_scale, int32_t* dev_status, void* stream) {
+  if (n < 0 || d_qk < 16 || d_qk % 16 != 0 || d_qk > dsa::kv_write_max_d() || page_size <= 0 || num_pages <= 0 ||
+      num_req <= 0 || bt_stride <= 0)
+    return DSA_ERR_INVALID_ARG;
+  if (num_pages > (int64_t)INT32_MAX / page_size) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0) return DSA_OK;
+  if (!rows || !req || !pos || !block_table || !kv || !kv_scale) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(rows) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
+  return from_cuda(dsa::launch_kv_write(rows, n, d_qk, req, pos, block_table, num_req, bt_stride, page_size,
+                                        num_pages, kv, kv_scale, dev_status, static_cast<cudaStream_t>(stream)));
+}

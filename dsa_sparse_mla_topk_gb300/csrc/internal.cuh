@@ -46,6 +46,13 @@ bool mla_tc_supported(const MlaArgs& a);
 size_t mla_tc_workspace_bytes(int32_t num_q, int32_t k);
 cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream);
 
+// KV cache write: FP8 E4M3 per-token quantisation + paged scatter (rows of up
+// to kv_write_max_d() values, a multiple of 16).
+int kv_write_max_d();
+cudaError_t launch_kv_write(const void* rows, int32_t n, int32_t d, const int32_t* req, const int32_t* pos,
+                            const int32_t* block_table, int32_t num_req, int32_t bt_stride, int32_t page_size,
+                            int64_t num_pages, uint8_t* kv, float* kv_scale, int32_t* status, cudaStream_t stream);
+
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t num_q,
                            int32_t heads, int32_t d_v, void* out, float* lse, cudaStream_t stream);
 

@@ -197,6 +197,37 @@ DSA_API dsa_status dsa_combine(const float* o_part, const float* lse_part, int32
                        int32_t num_heads, int32_t d_v, void* out, float* lse, void* stream);
 
 /*
+ * dsa_kv_write -- store new latent+rope KV rows into the paged FP8 cache: the
+ * write side of the rows that dsa_sparse_mla_fwd gathers.
+ *
+ * "Accelerating GLM-5.3-Flash on H200", section 2 "KV-only decode
+ * RadixCache": rows live in a paged pool, mapped per request by a block
+ * table (shared prefix pages appear in several tables).  SGLang cookbook page
+ * for GLM-5.3-Flash, "Keep the KV and DSA backends paired": the cache is FP8
+ * E4M3.  Row i is quantised with one fp32 scale per token: amax = max |x|,
+ * scale = amax / 448, byte_j = E4M3(x_j / scale) rounded to nearest even and
+ * saturated (both divisions IEEE fp32); an all-zero row stores scale 0 and
+ * zero bytes.  It is stored at slot = block_table[req[i]][pos[i] / page_size]
+ * * page_size + pos[i] % page_size.
+ *
+ *   rows         bf16 [n, d_qk] new rows (latent then rope), 16-byte aligned.
+ *   req, pos     int32 [n] request (0..num_req-1) and position of each row.
+ *   block_table  int32 [num_req, bt_stride] page ids (0..num_pages-1).
+ *   kv           uint8 [num_pages * page_size, d_qk] the cache, 16-byte
+ *                aligned; only the rows' slots are written.
+ *   kv_scale     fp32 [num_pages * page_size]; only the rows' slots are written.
+ *   d_qk         a multiple of 16, at most 2048.
+ * Errors: DSA_ERR_INVALID_ARG for bad sizes, null or misaligned pointers
+ * (nothing is launched); a request or page id out of range sets
+ * DSA_DEV_BAD_PAGE, a position outside the block table row sets
+ * DSA_DEV_BAD_INDEX, and that row is skipped.  Rows aimed at the same slot
+ * leave one of them there, unspecified which.  Asynchronous on `stream`.
+ */
+DSA_API dsa_status dsa_kv_write(const void* rows, int32_t n, int32_t d_qk, const int32_t* req, const int32_t* pos,
+                                const int32_t* block_table, int32_t num_req, int32_t bt_stride, int32_t page_size,
+                                int64_t num_pages, uint8_t* kv, float* kv_scale, int32_t* dev_status, void* stream);
+
+/*
  * Host-side planning helpers (no GPU needed).
  *
  * dsa_kv_tile_count: KV tiles of `tile` entries that cover an index row of

@@ -144,3 +144,22 @@ def test_python_binding_rejects_cpu_tensors(lib):
         dsa.topk_select(torch.zeros(2, 8), torch.zeros(2, dtype=torch.int32), 4)
     with pytest.raises(TypeError):
         dsa.topk_select(torch.zeros(2, 8, dtype=torch.float64), torch.zeros(2, dtype=torch.int32), 4)
+
+
+def _kvw(lib, **over):
+    a = dict(rows=FAKE, n=4, d=576, req=FAKE, pos=FAKE, bt=FAKE, num_req=1, bt_stride=4, P=64, num_pages=4, kv=FAKE,
+             sc=FAKE, st=None, stream=None)
+    a.update(over)
+    return lib.dsa_kv_write(a["rows"], a["n"], a["d"], a["req"], a["pos"], a["bt"], a["num_req"], a["bt_stride"],
+                            a["P"], a["num_pages"], a["kv"], a["sc"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(n=-1), 1), (dict(d=8), 1), (dict(d=584), 1), (dict(d=4096), 1), (dict(P=0), 1), (dict(num_pages=0), 1),
+    (dict(num_req=0), 1), (dict(bt_stride=0), 1), (dict(rows=None), 1), (dict(kv=None), 1), (dict(sc=None), 1),
+    (dict(req=None), 1), (dict(pos=None), 1), (dict(bt=None), 1), (dict(rows=MISALIGNED), 1),
+    (dict(kv=MISALIGNED), 1), (dict(num_pages=1 << 30, P=64), 2), (dict(n=0, rows=None), 0),
+])
+def test_kv_write_argument_checks(lib, over, expect):
+    """Every case returns before any CUDA call (fake device pointers)."""
+    assert _kvw(lib, **over) == expect
