@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--kv-write-rows", type=int, default=32768,
+                    help="rows of the separate KV-write measurement (0 = skip)")
     return ap.parse_args()
 
 
@@ -167,6 +169,24 @@ def dist_setup(args):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's `value` (the job's time is its slowest
+    rank's); `device` is where the collective's tensor lives."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank_step: int, steps: int, total_ms: float) -> float:
+    """Units all ranks processed per second: every rank does the same work
+    (weak scaling) and the job takes the slowest rank's time."""
+    return world * units_per_rank_step * steps / (total_ms / 1e3)
 
 
 def gpu_uuid(torch, dev):
@@ -335,13 +355,9 @@ def bench_ours(args):
     t_fwd = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
     t_comb = [evs[s][2].elapsed_time(evs[s][3]) for s in range(args.steps)]
     t_step = [evs[s][0].elapsed_time(evs[s][3]) for s in range(args.steps)]
-    total_ms = sum(t_step)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(t_step), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * w.num_q * args.steps / (total_ms / 1e3)
+    value = whole_job_rate(world, w.num_q, args.steps, total_ms)
 
     # ---- end to end through host buffers: copies timed every step ----
     e2e = None
@@ -374,16 +390,46 @@ def bench_ours(args):
             b.record(stream)
             b.synchronize()
             e_ms += a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * w.num_q * args.steps / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": whole_job_rate(world, w.num_q, args.steps, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
                "note": "KV cache resident in HBM; per-step inputs (q, scores, q_pos, q_req, block table) copied "
                        "from pinned host memory and out + lse read back, inside the timed region"}
     torch.cuda.synchronize(dev)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    # ---- the KV cache write path (a separate measurement, not in the step):
+    # n new bf16 rows quantised to FP8 and scattered through the block table,
+    # timed per call with the L2 flushed before each ----
+    kvw = None
+    if args.kv_write_rows > 0 and w.heads == 64:
+        n = args.kv_write_rows
+        g = torch.Generator(device=dev).manual_seed(5)
+        rows = torch.randn((n, w.dqk), generator=g, device=dev).to(torch.bfloat16)
+        kv_w = torch.zeros_like(inp.kv)
+        sc_w = torch.zeros_like(inp.kv_scale)
+        slots = inp.kv.shape[0]
+        perm = torch.randperm(slots, generator=g, device=dev)[:n].to(torch.int32)
+        bt_w = torch.arange(slots // w.page_size, dtype=torch.int32, device=dev)[None, :]
+        req_w = torch.zeros(n, dtype=torch.int32, device=dev)
+        for _ in range(max(1, args.warmup)):
+            dsa.kv_write(rows, req_w, perm, bt_w, kv_w, sc_w, page_size=w.page_size, dev_status=status, stream=stream)
+        t_kvw = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dsa.kv_write(rows, req_w, perm, bt_w, kv_w, sc_w, page_size=w.page_size, dev_status=status, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            t_kvw.append(a.elapsed_time(b))
+        ms = statistics.mean(t_kvw)
+        kbytes = n * (w.dqk * 2 + 4 + w.dqk + 4 + 4)  # rows read, req + pos read, codes + scale written
+        kvw = {"rows": n, "ms": ms, "rows_per_s": n / (ms / 1e3), "algorithmic_bytes": kbytes,
+               "achieved_gbs": kbytes / (ms / 1e3) / 1e9, "bound": "hbm",
+               "note": "random distinct slots of the workload's pool; L2 flushed before every call"}
+        torch.cuda.synchronize(dev)
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     if rank != 0:
         if world > 1:
@@ -391,6 +437,9 @@ def bench_ours(args):
         return 0
 
     peaks = read_peaks()
+    if kvw:
+        kvw["peak_gbs"] = peaks["hbm_gbs"]
+        kvw["frac"] = kvw["achieved_gbs"] / peaks["hbm_gbs"]
     fwd_ms = statistics.mean(t_fwd)
     src = os.path.join(ROOT, "dsa_sparse_mla_topk_gb300", "csrc",
                        "mla_tc.cu" if w.heads == 64 and os.environ.get("DSA_FORCE_SIMT") != "1" else "mla_simt.cu")
@@ -433,6 +482,7 @@ def bench_ours(args):
             "kernel_ms": {"topk": statistics.mean(t_topk), "sparse_mla_fwd": fwd_ms,
                           "combine": statistics.mean(t_comb)},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "kv_write": kvw,
             "clocks": sampler.summary() if sampler else None, "wall_s": wall}
     print(json.dumps(line), flush=True)
     if world > 1:
