@@ -15,6 +15,7 @@ import threading
 import torch
 
 __all__ = ["DsaError", "load_library", "topk_select", "sparse_mla_fwd", "combine", "sparse_mla_topk", "kv_write",
+           "PrefixCache",
            "kv_tile_count", "kv_tile_size", "pick_num_splits", "status_string", "EXPORTED_SYMBOLS",
            "DEV_BAD_QPOS", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT"]
 
@@ -26,8 +27,9 @@ DEV_BAD_QPOS, DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/dsa.h declares.
 EXPORTED_SYMBOLS = ("dsa_status_string", "dsa_version", "dsa_topk_select", "dsa_topk_workspace_size",
                     "dsa_sparse_mla_fwd", "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_fwd_noalloc",
-                    "dsa_combine", "dsa_kv_write", "dsa_kv_tile_count", "dsa_kv_tile_size",
-                    "dsa_pick_num_splits")
+                    "dsa_combine", "dsa_kv_write", "dsa_prefix_cache_create", "dsa_prefix_cache_destroy",
+                    "dsa_prefix_cache_acquire", "dsa_prefix_cache_release", "dsa_prefix_cache_stats",
+                    "dsa_kv_tile_count", "dsa_kv_tile_size", "dsa_pick_num_splits")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +74,16 @@ def load_library(path: str | None = None):
         lib.dsa_combine.restype = i32
         lib.dsa_kv_write.argtypes = [vp, i32, i32, vp, vp, vp, i32, i32, i32, i64, vp, vp, vp, vp]
         lib.dsa_kv_write.restype = i32
+        lib.dsa_prefix_cache_create.argtypes = [i32, i32]
+        lib.dsa_prefix_cache_create.restype = vp
+        lib.dsa_prefix_cache_destroy.argtypes = [vp]
+        lib.dsa_prefix_cache_destroy.restype = None
+        lib.dsa_prefix_cache_acquire.argtypes = [vp, vp, i64, vp, i32, vp, vp]
+        lib.dsa_prefix_cache_acquire.restype = i32
+        lib.dsa_prefix_cache_release.argtypes = [vp, vp, i32]
+        lib.dsa_prefix_cache_release.restype = i32
+        lib.dsa_prefix_cache_stats.argtypes = [vp, vp, vp, vp]
+        lib.dsa_prefix_cache_stats.restype = i32
         lib.dsa_kv_tile_count.argtypes = [i32, i32]
         lib.dsa_kv_tile_count.restype = i32
         lib.dsa_kv_tile_size.argtypes = [i32, i32, i32]
@@ -232,6 +244,58 @@ def kv_write(rows: torch.Tensor, req: torch.Tensor, pos: torch.Tensor, block_tab
           block_table.shape[1], page_size, kv.shape[0] // page_size, _p(kv), _p(kv_scale), _p(dev_status),
           _stream(stream))
     return kv, kv_scale
+
+
+class PrefixCache:
+    """KV-only prefix-sharing page allocator (host side): requests sharing
+    whole-page prefixes get the same page ids; see dsa_prefix_cache_* in
+    include/dsa.h."""
+
+    def __init__(self, page_size: int, num_pages: int):
+        self._lib = load_library()
+        self.page_size, self.num_pages = page_size, num_pages
+        self._h = self._lib.dsa_prefix_cache_create(page_size, num_pages)
+        if not self._h:
+            raise DsaError("dsa_prefix_cache_create", 1)
+
+    def acquire(self, tokens):
+        """int32 page ids of a request's tokens, and how many of the leading
+        ones were already cached (their KV rows need not be written)."""
+        import numpy as np
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        n_pages = (len(t) + self.page_size - 1) // self.page_size
+        bt = np.empty(max(1, n_pages), dtype=np.int32)
+        np_out, ns_out = ctypes.c_int32(0), ctypes.c_int32(0)
+        st = self._lib.dsa_prefix_cache_acquire(self._h, t.ctypes.data_as(ctypes.c_void_p), len(t),
+                                                bt.ctypes.data_as(ctypes.c_void_p), n_pages, ctypes.byref(np_out),
+                                                ctypes.byref(ns_out))
+        if st != 0:
+            raise DsaError("dsa_prefix_cache_acquire", st)
+        return bt[:np_out.value].copy(), ns_out.value
+
+    def release(self, block_table):
+        import numpy as np
+        bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+        st = self._lib.dsa_prefix_cache_release(self._h, bt.ctypes.data_as(ctypes.c_void_p), len(bt))
+        if st != 0:
+            raise DsaError("dsa_prefix_cache_release", st)
+
+    def stats(self):
+        """(pages referenced by live requests, pages cached, pages free)."""
+        a, b, c = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+        self._lib.dsa_prefix_cache_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+        return a.value, b.value, c.value
+
+    def close(self):
+        if self._h:
+            self._lib.dsa_prefix_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, *, d_latent: int, d_rope: int,

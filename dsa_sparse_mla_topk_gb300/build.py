@@ -1,4 +1,4 @@
-"""Build the CUDA library in-tree: csrc/*.cu -> libdsa.so (sm_103a only).
+"""Build the CUDA library in-tree: csrc/*.cu (+ host-only csrc/*.cpp) -> libdsa.so (sm_103a only).
 
 Each translation unit is compiled in parallel with nvcc, then linked into one
 shared library with a plain C ABI (include/dsa.h).  The library links the
@@ -35,7 +35,7 @@ def _flags(extra=()):
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():

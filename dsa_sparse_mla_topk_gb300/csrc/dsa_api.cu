@@ -47,6 +47,7 @@ const char* dsa_status_string(int32_t status) {
     case DSA_ERR_UNSUPPORTED_SHAPE: return "unsupported (heads, d_latent, d_rope)";
     case DSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case DSA_ERR_CUDA: return "CUDA error";
+    case DSA_ERR_OUT_OF_PAGES: return "page pool exhausted";
     default: return "unknown status";
   }
 }

@@ -61,7 +61,8 @@ typedef enum {
   DSA_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad alignment */
   DSA_ERR_UNSUPPORTED_SHAPE = 2, /* (heads, d_latent, d_rope) not compiled in */
   DSA_ERR_WORKSPACE_TOO_SMALL = 3,
-  DSA_ERR_CUDA = 4 /* a CUDA runtime call or kernel launch failed */
+  DSA_ERR_CUDA = 4, /* a CUDA runtime call or kernel launch failed */
+  DSA_ERR_OUT_OF_PAGES = 5 /* the page pool has no free or evictable page left */
 } dsa_status;
 
 /* Bits ORed into *dev_status by the kernels. */
@@ -226,6 +227,48 @@ DSA_API dsa_status dsa_combine(const float* o_part, const float* lse_part, int32
 DSA_API dsa_status dsa_kv_write(const void* rows, int32_t n, int32_t d_qk, const int32_t* req, const int32_t* pos,
                                 const int32_t* block_table, int32_t num_req, int32_t bt_stride, int32_t page_size,
                                 int64_t num_pages, uint8_t* kv, float* kv_scale, int32_t* dev_status, void* stream);
+
+/*
+ * KV-only prefix-sharing page allocator (host side, no GPU involved).
+ *
+ * "Accelerating GLM-5.3-Flash on H200", section 2 "KV-only decode
+ * RadixCache": requests sharing a prefix share its KV pages, so N requests
+ * with a common prefix of Lp tokens and private suffixes of Ls tokens occupy
+ * Lp + N·Ls slots instead of N·(Lp + Ls).  The unit of sharing is a whole
+ * page whose tokens, and all tokens before it, match (KV rows depend on the
+ * whole causal prefix); the block tables it returns are the ones
+ * dsa_kv_write and dsa_sparse_mla_fwd take.
+ *
+ * dsa_prefix_cache_create: a cache over a pool of num_pages pages of
+ *   page_size tokens (page ids 0..num_pages-1).  NULL on bad sizes or when
+ *   out of host memory.  The caller owns the handle (dsa_prefix_cache_destroy).
+ * dsa_prefix_cache_acquire: pages for a request of n_tokens token ids.
+ *   block_table (int32 [max_pages], host memory) receives ceil(n_tokens /
+ *   page_size) page ids: the first *n_shared are cached pages of the longest
+ *   matching whole-page prefix (their KV is already in the cache), the rest
+ *   are fresh (the caller writes their KV rows).  The request's new full pages
+ *   are cached for later requests; a partial last page stays private.  Every
+ *   page returned is referenced until released.  When no page is free,
+ *   unreferenced cached pages are evicted, least recently used first (leaves
+ *   of the prefix tree only); if none is left the call changes nothing and
+ *   returns DSA_ERR_OUT_OF_PAGES.  max_pages too small: DSA_ERR_INVALID_ARG.
+ * dsa_prefix_cache_release: drops the references of a block table acquire
+ *   returned (n_pages entries).  Private pages become free; cached pages stay
+ *   cached (reusable) until evicted.  An entry that is not a referenced page
+ *   returns DSA_ERR_INVALID_ARG and releases nothing.
+ * dsa_prefix_cache_stats: pages referenced by live requests, pages cached in
+ *   the prefix tree (referenced or not), free pages.
+ * The calls are thread-safe (one lock per cache).
+ */
+typedef struct dsa_prefix_cache dsa_prefix_cache;
+DSA_API dsa_prefix_cache* dsa_prefix_cache_create(int32_t page_size, int32_t num_pages);
+DSA_API void dsa_prefix_cache_destroy(dsa_prefix_cache* cache);
+DSA_API dsa_status dsa_prefix_cache_acquire(dsa_prefix_cache* cache, const int32_t* tokens, int64_t n_tokens,
+                                            int32_t* block_table, int32_t max_pages, int32_t* n_pages,
+                                            int32_t* n_shared);
+DSA_API dsa_status dsa_prefix_cache_release(dsa_prefix_cache* cache, const int32_t* block_table, int32_t n_pages);
+DSA_API dsa_status dsa_prefix_cache_stats(dsa_prefix_cache* cache, int32_t* pages_referenced, int32_t* pages_cached,
+                                          int32_t* pages_free);
 
 /*
  * Host-side planning helpers (no GPU needed).

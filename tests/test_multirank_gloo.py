@@ -43,7 +43,7 @@ def _rank_main(rank, world, port, results):
 
 def test_two_gloo_ranks_agree_on_the_slowest_time_and_the_whole_job_rate():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.start_processes(_rank_main, args=(world, _free_port(), results), nprocs=world, start_method="spawn",
                            join=True)
