@@ -318,3 +318,23 @@ def test_topk_sampling_fallbacks():
     qp = np.concatenate([q_pos] * 2)
     got = dsa.topk_select(torch.tensor(big, device="cuda"), torch.tensor(qp, device="cuda"), k)
     assert np.array_equal(host(got), oracle.topk(big, qp, k))
+
+
+def test_dcp_path_with_library_kernels_in_a_group_of_one():
+    """The DCP exchange code driving the library's kernels (local top-k,
+    candidate reselection, two-split Partial, Combine) in a group of one must
+    give the single-rank result."""
+    from dsa_sparse_mla_topk_gb300 import dcp
+    w = wl.Workload("dcp_gpu", 3, 2, 64, 512, 64, 3000, 0, 64, 2048, seed=37, ctx_per_req=(3000, 2500, 900))
+    inp = wl.make_inputs(w, device="cuda")
+    comp = dcp.library_compute(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, d_latent=w.d_latent,
+                               d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+    out, lse, idx = dcp.dcp_sparse_mla_topk(inp.scores, inp.q_pos, w.k, comp)
+    torch.cuda.synchronize()
+    rows = np.arange(w.num_q)
+    ref_idx, ref_out, ref_lse = oracle_rows(inp, rows)
+    assert np.array_equal(host(idx), ref_idx)
+    got = host(out.float()).astype(np.float64)
+    assert float(np.abs(got - ref_out).max()) <= MAX_ABS
+    assert float(np.linalg.norm(got - ref_out) / np.linalg.norm(ref_out)) <= REL_L2
+    assert float(np.abs(host(lse) - ref_lse).max()) <= LSE_ABS
