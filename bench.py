@@ -38,9 +38,10 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # capture, keyed by the SHA-1 of the kernel source it was taken on.  A stale
 # entry (the kernel changed since) is reported as null.
 TRAFFIC_BY_SOURCE: dict[str, dict] = {
-    # ncu --set full, second launch, decode_64k_prefix99.9: 49.05 MB read + 0.75 MB written
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, second launch,
+    # decode_64k_prefix99.9: 49,051,904 B read + 513,536 B written
     # (profiles/mla_tc_kernel_decode_64k_prefix99.9.md)
-    "19f21c5a8d04021fceb350d8121d9b8d937a5870": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49805312},
+    "fc7175a5ace561c212cec24b55beffdae6d83db8": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49565440},
 }
 
 

@@ -33,6 +33,8 @@ __device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
   return r;
 }
 
+// CH: 16-byte chunks each lane holds (rows of up to 32 * 8 * CH values)
+template <int CH>
 __global__ void __launch_bounds__(KVW_WARPS * 32)
     kv_write_kernel(const uint4* __restrict__ rows, int32_t n, int32_t d, const int32_t* __restrict__ req,
                     const int32_t* __restrict__ pos, const int32_t* __restrict__ block_table, int32_t num_req,
@@ -57,10 +59,10 @@ __global__ void __launch_bounds__(KVW_WARPS * 32)
   }
   const int64_t slot = (int64_t)page * page_size + p % page_size;
   const int nch = d / 8;  // 16-byte chunks of 8 bf16
-  uint4 v[KVW_MAX_CHUNKS];
+  uint4 v[CH];
   float amax = 0.f;
 #pragma unroll
-  for (int u = 0; u < KVW_MAX_CHUNKS; ++u) {
+  for (int u = 0; u < CH; ++u) {
     const int c = lane + 32 * u;
     if (c < nch) {
       v[u] = __ldg(rows + i * nch + c);
@@ -76,7 +78,7 @@ __global__ void __launch_bounds__(KVW_WARPS * 32)
   if (lane == 0) kv_scale[slot] = scale;
   uint2* dst = reinterpret_cast<uint2*>(kv + slot * d);
 #pragma unroll
-  for (int u = 0; u < KVW_MAX_CHUNKS; ++u) {
+  for (int u = 0; u < CH; ++u) {
     const int c = lane + 32 * u;
     if (c < nch) {
       const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
@@ -101,8 +103,10 @@ cudaError_t launch_kv_write(const void* rows, int32_t n, int32_t d, const int32_
                             int64_t num_pages, uint8_t* kv, float* kv_scale, int32_t* status, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n + KVW_WARPS - 1) / KVW_WARPS);
-  kv_write_kernel<<<grid, KVW_WARPS * 32, 0, stream>>>(static_cast<const uint4*>(rows), n, d, req, pos, block_table,
-                                                       num_req, bt_stride, page_size, num_pages, kv, kv_scale, status);
+  const int ch = (d / 8 + 31) / 32;  // chunks per lane
+  auto kern = ch <= 1 ? kv_write_kernel<1> : ch <= 3 ? kv_write_kernel<3> : kv_write_kernel<KVW_MAX_CHUNKS>;
+  kern<<<grid, KVW_WARPS * 32, 0, stream>>>(static_cast<const uint4*>(rows), n, d, req, pos, block_table, num_req,
+                                            bt_stride, page_size, num_pages, kv, kv_scale, status);
   return cudaGetLastError();
 }
 
