@@ -180,14 +180,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   d |= (uint64_t)swizzle << 61;
   return d;
 }
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-  return smem_desc(saddr, lbo_bytes, sbo_bytes, SWIZZLE_128B);
-}
-
-// Instruction descriptor of kind::f16 (and of kind::f8f6f4, where format 0
-// means E4M3 for A and B): A and B both bf16 (ab_bf16 = 1) or
-// both fp16 (0), fp32 D, shape M x N, A/B major-ness (0 = K-major, 1 =
-// MN-major).
+// Instruction descriptor with fp32 D: for kind::f16, A and B both bf16
+// (ab_bf16 = 1) or both fp16 (0); for kind::f8f6f4, format 0 means E4M3 for
+// A and B.  Shape M x N, A/B major-ness (0 = K-major, 1 = MN-major).
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major, int ab_bf16) {
   return (1u << 4)                         // D format: f32
          | ((uint32_t)ab_bf16 << 7)        // A format: f16 (0) / bf16 (1)
@@ -198,37 +193,11 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_majo
          | ((uint32_t)(M >> 4) << 24);     // M / 16
 }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc), issued by a single thread.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same MMA issued by a whole converged warp: elect.sync picks one lane
-// (the lowest) to issue.  Keeping the warp converged lets the descriptors stay
-// warp-uniform, which makes back-to-back issue several times cheaper than
-// issuing from inside a one-lane branch.
-__device__ __forceinline__ void mma_f16_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on the mbarrier when all previously issued tcgen05 async
-// operations of this thread have completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // kind::f8f6f4 MMA (K = 32 per instruction for 8-bit operands), issued by a
-// converged warp like mma_f16_ss_warp.
+// whole converged warp: elect.sync picks one lane (the lowest) to issue.
+// Keeping the warp converged lets the descriptors stay warp-uniform, which
+// makes back-to-back issue several times cheaper than issuing from inside a
+// one-lane branch.
 __device__ __forceinline__ void mma_f8_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                uint32_t accumulate) {
   asm volatile(
@@ -238,7 +207,9 @@ __device__ __forceinline__ void mma_f8_ss_warp(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
-// tcgen05.commit from the lane that mma_f16_ss_warp elects (whole warp converged).
+// tcgen05.commit from the lane that mma_f8_ss_warp elects (whole warp
+// converged): arrives once on the mbarrier when all tcgen05 async operations
+// that lane issued before have completed.
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
