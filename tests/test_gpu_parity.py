@@ -338,3 +338,39 @@ def test_dcp_path_with_library_kernels_in_a_group_of_one():
     assert float(np.abs(got - ref_out).max()) <= MAX_ABS
     assert float(np.linalg.norm(got - ref_out) / np.linalg.norm(ref_out)) <= REL_L2
     assert float(np.abs(host(lse) - ref_lse).max()) <= LSE_ABS
+
+
+def test_whole_step_replays_from_a_cuda_graph():
+    """top-k -> attention (resolve + attention kernels, programmatic dependent
+    launches) -> combine, captured once into a CUDA graph and replayed: every
+    replay gives the eager result bit for bit, for a split and an unsplit step."""
+    w = wl.Workload("graph_h64", 4, 2, 64, 512, 64, 3000, 2048, 64, 2048, seed=43)
+    inp = wl.make_inputs(w, device="cuda")
+    for splits in (1, 3):
+        kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale,
+                  num_splits=splits)
+        ws = dsa.sparse_mla_workspace_size(w.num_q, w.heads, w.d_latent, w.d_rope, w.k)
+        bufs = {"idx": torch.empty((w.num_q, w.k), dtype=torch.int32, device="cuda"),
+                "out": torch.empty((w.num_q, w.heads, w.d_latent), dtype=torch.bfloat16, device="cuda"),
+                "lse": torch.empty((w.num_q, w.heads), dtype=torch.float32, device="cuda"),
+                "workspace": torch.empty(ws, dtype=torch.uint8, device="cuda")}
+        if splits > 1:
+            bufs["o_part"] = torch.empty((splits, w.num_q, w.heads, w.d_latent), dtype=torch.float32, device="cuda")
+            bufs["lse_part"] = torch.empty((splits, w.num_q, w.heads), dtype=torch.float32, device="cuda")
+        out_e, lse_e, idx_e = dsa.sparse_mla_topk(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req,
+                                                  inp.q_pos, inp.scores, w.k, buffers=bufs, **kw)
+        ref = (out_e.clone(), lse_e.clone(), idx_e.clone())
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s), torch.cuda.graph(g, stream=s):
+            dsa.sparse_mla_topk(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, inp.q_pos, inp.scores, w.k,
+                                buffers=bufs, stream=s, **kw)
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(3):
+            for t in (bufs["out"], bufs["lse"], bufs["idx"]):
+                t.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(bufs["idx"], ref[2])
+            assert torch.equal(bufs["out"], ref[0]) and torch.equal(bufs["lse"], ref[1])
