@@ -139,18 +139,22 @@ def _call(fn: str, *args):
 
 
 def topk_select(scores: torch.Tensor, q_pos: torch.Tensor, k: int, idx: torch.Tensor | None = None,
-                dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """int32 [num_q, k] causal top-k positions (ascending, -1 padded)."""
+                dev_status: torch.Tensor | None = None, stream=None,
+                workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """int32 [num_q, k] causal top-k positions (ascending, -1 padded).
+    ``workspace`` (uint8, at least ``topk_workspace_size`` bytes) is allocated
+    when needed and not given."""
     _check(scores, "scores", torch.float32, 2)
     _check(q_pos, "q_pos", torch.int32, 1)
     num_q, ld = scores.shape
     if idx is None:
         idx = torch.empty((num_q, k), dtype=torch.int32, device=scores.device)
     _check(idx, "idx", torch.int32, 2)
-    ws_bytes = load_library().dsa_topk_workspace_size(num_q, ld, k)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=scores.device) if ws_bytes else None
-    _call("dsa_topk_select", _p(scores), ld, _p(q_pos), num_q, k, _p(idx), _p(ws), ws_bytes, _p(dev_status),
-          _stream(stream))
+    ws_bytes = topk_workspace_size(num_q, ld, k)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=scores.device)
+    _call("dsa_topk_select", _p(scores), ld, _p(q_pos), num_q, k, _p(idx), _p(workspace),
+          0 if workspace is None else workspace.numel(), _p(dev_status), _stream(stream))
     return idx
 
 
@@ -222,6 +226,11 @@ def combine(o_part: torch.Tensor, lse_part: torch.Tensor, out=None, lse=None, st
         lse = torch.empty((num_q, H), dtype=torch.float32, device=o_part.device)
     _call("dsa_combine", _p(o_part), _p(lse_part), S, num_q, H, dv, _p(out), _p(lse), _stream(stream))
     return out, lse
+
+
+def topk_workspace_size(num_q: int, ld: int, k: int) -> int:
+    """Scratch bytes dsa_topk_select needs (0 on the single-kernel path)."""
+    return int(load_library().dsa_topk_workspace_size(num_q, ld, k))
 
 
 def kv_write(rows: torch.Tensor, req: torch.Tensor, pos: torch.Tensor, block_table: torch.Tensor,
@@ -308,7 +317,8 @@ def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, 
     num_q, H, _ = q.shape
     if num_splits is None:
         num_splits = pick_num_splits(num_q, H, d_latent, d_rope, k)
-    idx = topk_select(scores, q_pos, k, idx=b.get("idx"), dev_status=dev_status, stream=stream)
+    idx = topk_select(scores, q_pos, k, idx=b.get("idx"), dev_status=dev_status, stream=stream,
+                      workspace=b.get("topk_workspace"))
     if num_splits == 1:
         out, lse = sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, idx, d_latent=d_latent, d_rope=d_rope,
                                   page_size=page_size, softmax_scale=softmax_scale, num_splits=1, out=b.get("out"),

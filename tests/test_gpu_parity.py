@@ -374,3 +374,27 @@ def test_whole_step_replays_from_a_cuda_graph():
             torch.cuda.synchronize()
             assert torch.equal(bufs["idx"], ref[2])
             assert torch.equal(bufs["out"], ref[0]) and torch.equal(bufs["lse"], ref[1])
+
+
+def test_topk_edges_bit_exact():
+    """Rows around every threshold of the kernel (k, the 3072-position limit
+    under which every position is a candidate, 8192-position boundaries),
+    misaligned rows (odd row stride), heavy ties, and all the large scores
+    packed into one stretch of a row must all match the oracle."""
+    k = 2048
+    ld = 70001  # odd: most rows start off a 16-byte boundary
+    q_pos = np.array([100, 2047, 2048, 3071, 3072, 3073, 8191, 8192, 8193, 16383, 50000, 70000, 70000, 69999],
+                     dtype=np.int32)
+    n = len(q_pos)
+    g = torch.Generator().manual_seed(51)
+    sc = torch.randn((n, ld), generator=g)
+    sc[1] = torch.randint(0, 4, (ld,), generator=g).float()        # heavy ties
+    sc[11, 20000:28192] += 50.0                                    # one chunk holds everything large
+    sc[12, ::3] = sc[12, 0]                                        # ties across the whole row
+    scores = sc.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = dsa.topk_select(scores, torch.from_numpy(q_pos).cuda(), k, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.topk(sc.numpy(), q_pos, k)
+    assert np.array_equal(host(idx), ref)
