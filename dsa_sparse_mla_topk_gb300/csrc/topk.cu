@@ -43,8 +43,9 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix sum of one value per thread over the block; *total gets
-// the block sum.  `warp_buf` holds 32 words of shared memory.
+// Exclusive prefix sum of one value per thread over a block of NTH threads;
+// *total gets the block sum.  `warp_buf` holds 32 words of shared memory.
+template <int NTH = NT>
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* total, uint32_t* warp_buf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
@@ -56,17 +57,17 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
   if (lane == 31) warp_buf[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = lane < NT / 32 ? warp_buf[lane] : 0u;
+    uint32_t w = lane < NTH / 32 ? warp_buf[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    if (lane < NT / 32) warp_buf[lane] = w;
+    if (lane < NTH / 32) warp_buf[lane] = w;
   }
   __syncthreads();
   const uint32_t before = warp > 0 ? warp_buf[warp - 1] : 0u;
-  *total = warp_buf[NT / 32 - 1];
+  *total = warp_buf[NTH / 32 - 1];
   __syncthreads();
   return before + x - v;
 }
@@ -277,8 +278,9 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
     __syncthreads();
     uint32_t t_lo = 0;
     if (vis > MCAP / 2 && ns > 0) {
-      const double expect = (double)k * (double)ns / (double)vis;
-      uint32_t need = (uint32_t)(expect * 1.25) + 16u;
+      // (fp32: fp64 arithmetic in every thread costs microseconds here)
+      const float expect = (float)k * (float)ns / (float)vis;
+      uint32_t need = (uint32_t)(expect * 1.25f) + 16u;
       if (need > ns) need = ns;
       uint32_t bin, above, count;
       find_bin(hist, HBINS, need > 0 ? need : 1u, warp_buf, sel, bin, above, count);
@@ -380,6 +382,323 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Rows of up to 65,536 visible positions: one CTA of 512 threads per row,
+// two CTAs per SM (80 KB of shared memory each), so that one CTA streams
+// while the other selects.
+//   0. An L2 bulk prefetch of the whole row is issued first.
+//   1. A 1/16 sample (the first 8 of every 128 positions) places a lower
+//      12-bit threshold T_lo as in the cluster kernel.
+//   2. One streaming pass screens every key against T_lo in registers.  Each
+//      warp appends its candidates (full key, position) to its own segment
+//      of a shared-memory list through ballots: no atomics, no block-wide
+//      synchronisation.
+//   3. The k-th largest candidate key is found exactly by radix passes over
+//      (key - min key), up to 11 bits each, from the highest significant bit.
+//   4. The keys above it and the keys equal to it are marked in two position
+//      bitmaps; one ordered pass over the bitmaps writes the positions above,
+//      plus the lowest-positioned equal ones, in ascending order.
+// If the sample misleads (fewer than k candidates, or a full segment), the
+// CTA falls back to the exact multi-pass radix select over the row in global
+// memory, so the result never depends on the score distribution.
+constexpr int RNT = 512;                 // threads per CTA
+constexpr int RWARPS = RNT / 32;
+constexpr int RMAXV = 65536;             // visible positions (positions fit in 16 bits)
+constexpr int RWCAP = 512;               // candidates one warp can hold
+constexpr int RLCAP = RWARPS * RWCAP;    // 8192
+constexpr int RALL = 4096;               // rows this short take every position as a candidate
+constexpr int RDEPTH = 8;                // float4 loads in flight per thread
+constexpr int RWORDS = RMAXV / 32;       // bitmap words
+constexpr size_t RSMEM = sizeof(uint32_t) * (RLCAP + HBINS + 2 * RWORDS) + sizeof(uint16_t) * RLCAP;
+static_assert(RNT * SAMPLE_BLOCK == RMAXV, "one sample block per thread must cover a row");
+
+__device__ __forceinline__ void l2_prefetch_bulk(uintptr_t addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
+
+// find_bin with three barriers instead of five.  It skips the barriers that
+// protect warp_buf and sel from the next call, so consecutive calls must be
+// separated by at least one other barrier.
+__device__ __forceinline__ void find_bin_fast(const uint32_t* hist, int nbins, uint32_t krem, uint32_t* warp_buf,
+                                              uint32_t* sel, uint32_t& bin, uint32_t& above, uint32_t& count) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = nbins / NT;  // bins per thread, highest bins to thread 0
+  uint32_t c[HBINS / NT];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int t = 0; t < HBINS / NT; ++t) {
+    c[t] = t < per ? hist[nbins - 1 - (threadIdx.x * per + t)] : 0u;
+    sum += c[t];
+  }
+  uint32_t x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_buf[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < NT / 32 ? warp_buf[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < NT / 32) warp_buf[lane] = w;
+  }
+  __syncthreads();
+  uint32_t acc = (warp > 0 ? warp_buf[warp - 1] : 0u) + x - sum;
+#pragma unroll
+  for (int t = 0; t < HBINS / NT; ++t) {
+    if (t < per && acc < krem && krem <= acc + c[t]) {
+      sel[0] = nbins - 1 - (threadIdx.x * per + t);
+      sel[1] = acc;
+      sel[2] = c[t];
+    }
+    acc += c[t];
+  }
+  __syncthreads();
+  bin = sel[0], above = sel[1], count = sel[2];
+}
+
+__global__ void __launch_bounds__(RNT, 2)
+    topk_row_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ q_pos, int32_t k,
+                    int32_t* __restrict__ idx, int32_t* status) {
+  extern __shared__ __align__(16) uint32_t rsm[];
+  uint32_t* ckey = rsm;                                              // [RLCAP] candidate keys
+  uint32_t* hist = ckey + RLCAP;                                     // [HBINS]
+  uint32_t* above_bm = hist + HBINS;                                 // [RWORDS] keys above the threshold
+  uint32_t* equal_bm = above_bm + RWORDS;                            // [RWORDS] keys equal to it
+  uint16_t* cpos = reinterpret_cast<uint16_t*>(equal_bm + RWORDS);   // [RLCAP] candidate positions
+  __shared__ uint32_t warp_buf[32];
+  __shared__ uint32_t sel[4];
+  __shared__ uint32_t minmax[2];
+  __shared__ uint32_t wcount[RWARPS];
+
+  // the next kernel on the stream may be scheduled now; it waits for this
+  // grid's results before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  int32_t* out = idx + row * (int64_t)k;
+  const int64_t p = q_pos[row];
+  if (p < 0 || p >= ld) {
+    if (tid == 0) report(status, DSA_DEV_BAD_QPOS);
+    for (int j = tid; j < k; j += RNT) out[j] = -1;
+    return;
+  }
+  const int vis = (int)(p + 1);  // <= ld <= RMAXV
+  if (vis <= k) {
+    for (int j = tid; j < k; j += RNT) out[j] = j < vis ? j : -1;
+    return;
+  }
+  const float* s = scores + row * ld;
+  const int head0 = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(s) & 15u)) & 15u) >> 2);
+  const int h0 = head0 < vis ? head0 : vis;  // positions before the first 16-byte boundary
+  const int nv4 = (vis - h0) >> 2;           // whole float4s after them
+  const float4* s4 = reinterpret_cast<const float4*>(s + h0);
+  constexpr int HB = RDEPTH / 2;  // float4s per thread in a half-batch
+  auto load = [&](float4 (&v)[HB], int base) {
+#pragma unroll
+    for (int d = 0; d < HB; ++d) {
+      const int f = base + d * RNT + tid;
+      v[d] = f < nv4 ? __ldg(s4 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+
+  // ---- 0. loads in this order: a 1/16 sample (the first 8 of every 128
+  // positions), the whole row into L2 (eight 16-byte-aligned pieces inside
+  // it), the first half-batch of the stream ----
+  const bool sampled = vis > RALL;
+  const int blk = tid * SAMPLE_BLOCK;  // one sample block per thread covers a row
+  float sv[SAMPLE_RUN];
+#pragma unroll
+  for (int t = 0; t < SAMPLE_RUN; ++t) sv[t] = sampled && blk + t < vis ? __ldg(s + blk + t) : 0.f;
+  if (tid < 8) {
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(s) + 15u) & ~uintptr_t(15);
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(s + vis) & ~uintptr_t(15);
+    if (a1 > a0) {
+      const uintptr_t piece = ((a1 - a0) / 8 + 15u) & ~uintptr_t(15);
+      const uintptr_t b0 = a0 + piece * (uintptr_t)tid;
+      const uintptr_t b1 = b0 + piece < a1 ? b0 + piece : a1;
+      if (b1 > b0) l2_prefetch_bulk(b0, (uint32_t)(b1 - b0));
+    }
+  }
+  for (int b = tid; b < HBINS; b += RNT) hist[b] = 0u;
+  for (int b = tid; b < 2 * RWORDS; b += RNT) above_bm[b] = 0u;
+  if (tid == 0) minmax[0] = 0xffffffffu, minmax[1] = 0u;
+  __syncthreads();
+
+  // ---- 1. the lower threshold from the sample ----
+  uint32_t t_lo = 0u;
+  if (sampled) {
+#pragma unroll
+    for (int t = 0; t < SAMPLE_RUN; ++t)
+      if (blk + t < vis) atomicAdd(&hist[score_key(sv[t]) >> 20], 1u);
+    const uint32_t ns = (uint32_t)(vis / SAMPLE_BLOCK) * SAMPLE_RUN + (uint32_t)min(vis % SAMPLE_BLOCK, SAMPLE_RUN);
+    const float expect = (float)k * (float)ns / (float)vis;
+    uint32_t need = (uint32_t)(expect * 1.25f) + 16u;
+    if (need > ns) need = ns;
+    __syncthreads();
+    uint32_t bin, above, count;
+    find_bin_fast(hist, HBINS, need, warp_buf, sel, bin, above, count);
+    t_lo = bin << 20;
+    for (int b = tid; b < HBINS; b += RNT) hist[b] = 0u;  // read by now; both radix buffers start cleared
+  }
+
+  // ---- 2. one streaming pass; each warp lists its candidates ----
+  uint32_t wcnt = 0;  // the same in every lane of the warp
+  uint32_t* wkey = ckey + warp * RWCAP;
+  uint16_t* wpos = cpos + warp * RWCAP;
+  auto push = [&](bool cand, uint32_t key, int pos) {
+    const uint32_t b = __ballot_sync(0xffffffffu, cand);
+    if (b) {
+      const uint32_t r = wcnt + __popc(b & ((1u << lane) - 1u));
+      if (cand && r < (uint32_t)RWCAP) {
+        wkey[r] = key;
+        wpos[r] = (uint16_t)pos;
+      }
+      wcnt += __popc(b);
+    }
+  };
+  auto screen = [&](const float4 (&v)[HB], int base) {
+#pragma unroll
+    for (int d = 0; d < HB; ++d) {
+      const int f = base + d * RNT + tid;
+      const bool ok = f < nv4;
+      const int e = h0 + 4 * f;
+      const uint32_t k0 = score_key(v[d].x), k1 = score_key(v[d].y);
+      const uint32_t k2 = score_key(v[d].z), k3 = score_key(v[d].w);
+      push(ok && k0 >= t_lo, k0, e);
+      push(ok && k1 >= t_lo, k1, e + 1);
+      push(ok && k2 >= t_lo, k2, e + 2);
+      push(ok && k3 >= t_lo, k3, e + 3);
+    }
+  };
+  // the loads of one half-batch are in flight while the other is screened
+  float4 va[HB], vb[HB];
+  load(va, 0);
+  for (int base = 0; base < nv4; base += 2 * RNT * HB) {
+    load(vb, base + RNT * HB);
+    screen(va, base);
+    load(va, base + 2 * RNT * HB);
+    screen(vb, base + RNT * HB);
+  }
+  if (warp == 0) {  // the unaligned head (lanes 0-2) and tail (lanes 4-6)
+    const int nt = vis - h0 - 4 * nv4;
+    const int pe = lane < h0 ? lane : (lane >= 4 && lane - 4 < nt ? h0 + 4 * nv4 + lane - 4 : -1);
+    const uint32_t key = pe >= 0 ? score_key(__ldg(s + pe)) : 0u;
+    push(pe >= 0 && key >= t_lo, key, pe);
+  }
+  if (lane == 0) wcount[warp] = wcnt;
+  __syncthreads();
+  uint32_t total = 0;
+  bool full = false;
+#pragma unroll
+  for (int w = 0; w < RWARPS; ++w) {
+    total += wcount[w];
+    full |= wcount[w] > (uint32_t)RWCAP;
+  }
+  if (full || total < (uint32_t)k) {
+    // the sample misled: exact selection over the row in global memory
+    select_exact<true>(s, nullptr, nullptr, vis, (uint32_t)k, out, hist, warp_buf, sel);
+    return;
+  }
+
+  // ---- 3. exact k-th largest key among the candidates ----
+  // thread t holds entry t of every warp's segment
+  uint32_t have = 0;  // bit w: entry t of segment w exists
+#pragma unroll
+  for (int w = 0; w < RWARPS; ++w)
+    if ((uint32_t)tid < wcount[w]) have |= 1u << w;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+  for (int w = 0; w < RWARPS; ++w) {
+    if ((have >> w) & 1u) {
+      const uint32_t key = ckey[w * RWCAP + tid];
+      lo = min(lo, key);
+      hi = max(hi, key);
+    }
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    atomicMin(&minmax[0], lo);
+    atomicMax(&minmax[1], hi);
+  }
+  __syncthreads();
+  // radix state over u = key - kmin: every u with (u & mask) > prefix is
+  // taken, and the first krem by position with (u & mask) == prefix
+  const uint32_t kmin = minmax[0];
+  uint32_t top = 32 - __clz(minmax[1] - kmin);  // significant bits of (key - kmin)
+  uint32_t prefix = 0, mask = 0, krem = (uint32_t)k;
+  for (int pass = 0; top > 0; ++pass) {
+    uint32_t* h = hist + (pass & 1) * 2048;  // each buffer is cleared while the other counts
+    const int sh = top > 11 ? (int)top - 11 : 0;
+    const uint32_t dm = (1u << (top - sh)) - 1u;
+#pragma unroll
+    for (int w = 0; w < RWARPS; ++w) {
+      if ((have >> w) & 1u) {
+        const uint32_t u = ckey[w * RWCAP + tid] - kmin;
+        if ((u & mask) == prefix) atomicAdd(&h[(u >> sh) & dm], 1u);
+      }
+    }
+    __syncthreads();
+    uint32_t bin, above, count;
+    find_bin_fast(h, 2048, krem, warp_buf, sel, bin, above, count);
+    for (int b = tid; b < 2048; b += RNT) h[b] = 0u;
+    prefix |= bin << sh;
+    mask |= dm << sh;
+    krem -= above;
+    top = sh;
+    if (count == krem) break;  // the whole bin is taken
+  }
+
+  // ---- 4. mark, then write in position order ----
+#pragma unroll
+  for (int w = 0; w < RWARPS; ++w) {
+    if ((have >> w) & 1u) {
+      const uint32_t mk = (ckey[w * RWCAP + tid] - kmin) & mask;
+      const uint32_t q = cpos[w * RWCAP + tid];
+      if (mk > prefix) atomicOr(&above_bm[q >> 5], 1u << (q & 31));
+      else if (mk == prefix) atomicOr(&equal_bm[q >> 5], 1u << (q & 31));
+    }
+  }
+  __syncthreads();
+  constexpr int WPT = RWORDS / RNT;  // bitmap words per thread: positions 32*WPT*t onwards
+  uint32_t aw[WPT], ew[WPT];
+  uint32_t n_above = 0, n_eq = 0;
+#pragma unroll
+  for (int j = 0; j < WPT; ++j) {
+    aw[j] = above_bm[tid * WPT + j];
+    ew[j] = equal_bm[tid * WPT + j];
+    n_above += __popc(aw[j]);
+    n_eq += __popc(ew[j]);
+  }
+  // one scan of (keys above, equal keys) packed in 16 bits each (both < 65536)
+  uint32_t packed_total;
+  const uint32_t before = block_exclusive_scan((n_above << 16) | n_eq, &packed_total, warp_buf);
+  const uint32_t eq_before = before & 0xffffu;
+  uint32_t o = (before >> 16) + min(eq_before, krem);  // output slot of this thread's first position
+  uint32_t rank = eq_before;
+#pragma unroll
+  for (int j = 0; j < WPT; ++j) {
+    uint32_t e = ew[j];
+    while (e && rank < krem) {
+      aw[j] |= e & (~e + 1u);  // the lowest equal key still unclaimed
+      e &= e - 1u;
+      ++rank;
+    }
+    uint32_t a = aw[j];
+    while (a && o < (uint32_t)k) {
+      const int b = __ffs(a) - 1;
+      a &= a - 1u;
+      out[o++] = (tid * WPT + j) * 32 + b;
+    }
+  }
+}
+
 template <int C>
 cudaError_t launch_c(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k, int32_t* idx,
                      int32_t* dev_status, cudaStream_t stream) {
@@ -406,6 +725,12 @@ int topk_cluster_size(int32_t num_q, int64_t ld, int num_sms) {
 cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
                         int32_t* idx, int32_t* dev_status, cudaStream_t stream) {
   if (num_q == 0) return cudaSuccess;
+  if (ld <= RMAXV) {
+    cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RSMEM);
+    if (e != cudaSuccess) return e;
+    topk_row_kernel<<<(unsigned)num_q, RNT, RSMEM, stream>>>(scores, ld, q_pos, k, idx, dev_status);
+    return cudaGetLastError();
+  }
   const int sms = device_sm_count();
   switch (topk_cluster_size(num_q, ld, sms)) {
     case 8: return launch_c<8>(scores, ld, q_pos, num_q, k, idx, dev_status, stream);

@@ -294,11 +294,14 @@ def test_large_logit_range_triggers_rescale():
     assert float(np.abs(host(lse) - ref_lse).max()) <= LSE_ABS
 
 
-def test_topk_sampling_fallbacks():
+@pytest.mark.parametrize("ld", [70000, 65536, 65531])
+def test_topk_sampling_fallbacks(ld):
     """Rows on which the sampled threshold cannot work (all scores equal: too
     many candidates; high scores only at unsampled positions: too few) take
-    the exact fallback and must still match the oracle bit for bit."""
-    ld, k = 70000, 2048
+    the exact fallback and must still match the oracle bit for bit.  Rows of
+    up to 65,536 positions run the row-in-shared-memory kernel, longer ones
+    the cluster kernel; 65531 makes most rows start off a 16-byte boundary."""
+    k = 2048
     rows = []
     rows.append(np.full(ld, 0.5, dtype=np.float32))                       # all equal
     r = np.random.default_rng(4).standard_normal(ld).astype(np.float32)
@@ -309,8 +312,15 @@ def test_topk_sampling_fallbacks():
     r2[(pos % 128) < 8] += 10.0                                            # sampled positions high
     rows.append(r2)
     rows.append(np.sort(np.random.default_rng(6).standard_normal(ld).astype(np.float32))[::-1].copy())
+    # the row kernel samples every 16th position
+    r3 = np.random.default_rng(7).standard_normal(ld).astype(np.float32)
+    r3[(pos % 16) != 0] += 10.0                                            # unsampled positions high
+    rows.append(r3)
+    r4 = np.random.default_rng(8).standard_normal(ld).astype(np.float32)
+    r4[(pos % 16) == 0] += 10.0                                            # sampled positions high
+    rows.append(r4)
     scores = np.stack(rows)
-    q_pos = np.array([ld - 1, ld - 1, ld - 100, ld - 7], dtype=np.int32)
+    q_pos = np.array([ld - 1, ld - 1, ld - 100, ld - 7, ld - 1, ld - 3], dtype=np.int32)
     got = dsa.topk_select(torch.tensor(scores, device="cuda"), torch.tensor(q_pos, device="cuda"), k)
     assert np.array_equal(host(got), oracle.topk(scores, q_pos, k))
     # the same rows in a batch big enough to use multi-CTA clusters
@@ -376,21 +386,27 @@ def test_whole_step_replays_from_a_cuda_graph():
             assert torch.equal(bufs["out"], ref[0]) and torch.equal(bufs["lse"], ref[1])
 
 
-def test_topk_edges_bit_exact():
-    """Rows around every threshold of the kernel (k, the 3072-position limit
-    under which every position is a candidate, 8192-position boundaries),
-    misaligned rows (odd row stride), heavy ties, and all the large scores
-    packed into one stretch of a row must all match the oracle."""
+@pytest.mark.parametrize("ld", [70001, 65535])
+def test_topk_edges_bit_exact(ld):
+    """Rows around every threshold of the kernels (k, the limits under which
+    every position is a candidate, 8192-position boundaries), misaligned rows
+    (odd row stride), heavy ties, all the large scores packed into one
+    stretch of a row, and exact ties straddling rank k must all match the
+    oracle.  ld = 70001 runs the cluster kernel, 65535 the
+    row-in-shared-memory kernel."""
     k = 2048
-    ld = 70001  # odd: most rows start off a 16-byte boundary
-    q_pos = np.array([100, 2047, 2048, 3071, 3072, 3073, 8191, 8192, 8193, 16383, 50000, 70000, 70000, 69999],
-                     dtype=np.int32)
+    q_pos = np.array([100, 2047, 2048, 3071, 3072, 3073, 8191, 8192, 8193, 16383, 50000, ld - 1, ld - 1, ld - 2,
+                      ld - 3], dtype=np.int32)
     n = len(q_pos)
     g = torch.Generator().manual_seed(51)
     sc = torch.randn((n, ld), generator=g)
     sc[1] = torch.randint(0, 4, (ld,), generator=g).float()        # heavy ties
     sc[11, 20000:28192] += 50.0                                    # one chunk holds everything large
     sc[12, ::3] = sc[12, 0]                                        # ties across the whole row
+    # 40 exact copies of the value ranked k - 10 among the visible ones
+    vis = int(q_pos[14]) + 1
+    v = torch.sort(sc[14, :vis], descending=True).values[k - 10]
+    sc[14, torch.randperm(vis, generator=g)[:40]] = v
     scores = sc.cuda()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     idx = dsa.topk_select(scores, torch.from_numpy(q_pos).cuda(), k, dev_status=status)
