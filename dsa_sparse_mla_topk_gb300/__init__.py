@@ -143,7 +143,8 @@ def topk_select(scores: torch.Tensor, q_pos: torch.Tensor, k: int, idx: torch.Te
                 workspace: torch.Tensor | None = None) -> torch.Tensor:
     """int32 [num_q, k] causal top-k positions (ascending, -1 padded).
     ``workspace`` (uint8, at least ``topk_workspace_size`` bytes) is allocated
-    when needed and not given."""
+    when the sliced path for rows longer than 65,536 positions applies and
+    none is given; an empty tensor selects the in-place path instead."""
     _check(scores, "scores", torch.float32, 2)
     _check(q_pos, "q_pos", torch.int32, 1)
     num_q, ld = scores.shape
@@ -229,7 +230,7 @@ def combine(o_part: torch.Tensor, lse_part: torch.Tensor, out=None, lse=None, st
 
 
 def topk_workspace_size(num_q: int, ld: int, k: int) -> int:
-    """Scratch bytes dsa_topk_select needs (0 on the single-kernel path)."""
+    """Workspace bytes dsa_topk_select can use (0 when no workspace applies)."""
     return int(load_library().dsa_topk_workspace_size(num_q, ld, k))
 
 

@@ -96,8 +96,7 @@ size_t dsa_sparse_mla_workspace_size(int32_t num_q, int32_t num_heads, int32_t d
 }
 
 size_t dsa_topk_workspace_size(int32_t num_q, int64_t ld_scores, int32_t k) {
-  (void)num_q, (void)ld_scores, (void)k;
-  return 0;
+  return dsa::topk_workspace_bytes(num_q, ld_scores, k);
 }
 
 dsa_status dsa_topk_select(const float* scores, int64_t ld_scores, const int32_t* q_pos, int32_t num_q,
@@ -106,10 +105,12 @@ dsa_status dsa_topk_select(const float* scores, int64_t ld_scores, const int32_t
   if (num_q < 0 || k <= 0 || ld_scores <= 0) return DSA_ERR_INVALID_ARG;
   if (num_q == 0) return DSA_OK;
   if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
-  if (workspace_bytes < dsa_topk_workspace_size(num_q, ld_scores, k)) return DSA_ERR_WORKSPACE_TOO_SMALL;
-  (void)workspace;
-  return from_cuda(dsa::launch_topk(scores, ld_scores, q_pos, num_q, k, idx, dev_status,
-                                    static_cast<cudaStream_t>(stream)));
+  // the workspace is optional: none selects the in-place path; a partial one is an error
+  const size_t need = dsa_topk_workspace_size(num_q, ld_scores, k);
+  if (workspace_bytes > 0 && workspace_bytes < need) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes > 0 && !workspace) return DSA_ERR_INVALID_ARG;
+  return from_cuda(dsa::launch_topk(scores, ld_scores, q_pos, num_q, k, idx, workspace, workspace_bytes,
+                                    dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_scale, int64_t num_pages,

@@ -10,7 +10,11 @@ namespace dsa {
 
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
-                        int32_t* idx, int32_t* dev_status, cudaStream_t stream);
+                        int32_t* idx, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        cudaStream_t stream);
+// Workspace bytes the sliced top-k of rows longer than 65,536 positions uses
+// (0 when it does not apply).
+size_t topk_workspace_bytes(int32_t num_q, int64_t ld, int32_t k);
 // CTAs per top-k row (a thread-block cluster) for this launch.
 int topk_cluster_size(int32_t num_q, int64_t ld, int num_sms);
 

@@ -101,13 +101,14 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32
 }
 
 // Exact selection over n keys with positions (keys/pos in any memory, in
-// ascending position order): writes the k chosen positions ascending.
+// ascending position order): emit(slot, position) receives the k chosen
+// positions in ascending order, slot 0..k-1.
 // Radix passes of up to 11 bits run over (key - kmin) from its highest set
 // bit down, so the bins spread over the keys' actual range (candidate keys
 // share their top bits; fixed digits would pile them into a few bins).
-template <bool GLOBAL_ROW>
+template <bool GLOBAL_ROW, class Emit>
 __device__ void select_exact(const float* row_scores, const uint32_t* keys, const int32_t* pos, int64_t n, uint32_t k,
-                             int32_t* out, uint32_t* hist, uint32_t* warp_buf, uint32_t* sel) {
+                             Emit emit, uint32_t* hist, uint32_t* warp_buf, uint32_t* sel) {
   auto key_at = [&](int64_t e) -> uint32_t { return GLOBAL_ROW ? score_key(row_scores[e]) : keys[e]; };
   auto pos_at = [&](int64_t e) -> int32_t { return GLOBAL_ROW ? (int32_t)e : pos[e]; };
   uint32_t kmin = 0, top = 32;
@@ -179,7 +180,7 @@ __device__ void select_exact(const float* row_scores, const uint32_t* keys, cons
     uint32_t o = written + block_exclusive_scan(__popc(take), &take_total, warp_buf);
 #pragma unroll
     for (int t = 0; t < PER; ++t)
-      if (((take >> t) & 1u) && o < k) out[o++] = pos_at(e0 + t);
+      if (((take >> t) & 1u) && o < k) emit(o++, pos_at(e0 + t));
     ties_before += eq_total;
     written += take_total;
   }
@@ -376,9 +377,11 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
   cluster.sync();  // the other CTAs' shared memory is no longer read
   if (rank != 0) return;
   if (!fallback) {
-    select_exact<false>(nullptr, mkey, mpos, vars[3], (uint32_t)k, out, hist, warp_buf, sel);
+    select_exact<false>(nullptr, mkey, mpos, vars[3], (uint32_t)k, [&](uint32_t o, int32_t q) { out[o] = q; },
+                        hist, warp_buf, sel);
   } else {
-    select_exact<true>(s, nullptr, nullptr, vis, (uint32_t)k, out, hist, warp_buf, sel);
+    select_exact<true>(s, nullptr, nullptr, vis, (uint32_t)k, [&](uint32_t o, int32_t q) { out[o] = q; }, hist,
+                       warp_buf, sel);
   }
 }
 
@@ -462,9 +465,23 @@ __device__ __forceinline__ void find_bin_fast(const uint32_t* hist, int nbins, u
   bin = sel[0], above = sel[1], count = sel[2];
 }
 
+// What one CTA of topk_row_kernel does:
+//   ROW_PLAIN  the top k of a row of up to RMAXV positions, into idx;
+//   ROW_SLICE  the top k of slice blockIdx.x % nslices (RMAXV positions) of a
+//              longer row, as (score, position) into a k-entry block of the
+//              workspace: ascending positions, then (-NaN, -1) padding, which
+//              ranks below every number;
+//   ROW_MERGE  the top k of a long row from the union of its slices' blocks.
+//              The blocks are in slice order and each is ascending, so union
+//              order is position order and ties still go to the lower position.
+enum RowMode { ROW_PLAIN = 0, ROW_SLICE = 1, ROW_MERGE = 2 };
+constexpr uint32_t PAD_SCORE_BITS = 0xffc00000u;  // -NaN: its key is below every number's
+
+template <int MODE>
 __global__ void __launch_bounds__(RNT, 2)
     topk_row_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ q_pos, int32_t k,
-                    int32_t* __restrict__ idx, int32_t* status) {
+                    int32_t* __restrict__ idx, int32_t* status, float* __restrict__ ws_score,
+                    int32_t* __restrict__ ws_pos, int nslices) {
   extern __shared__ __align__(16) uint32_t rsm[];
   uint32_t* ckey = rsm;                                              // [RLCAP] candidate keys
   uint32_t* hist = ckey + RLCAP;                                     // [HBINS]
@@ -480,20 +497,58 @@ __global__ void __launch_bounds__(RNT, 2)
   // grid's results before reading them
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t row = blockIdx.x;
-  int32_t* out = idx + row * (int64_t)k;
+  const int64_t row = MODE == ROW_SLICE ? blockIdx.x / nslices : blockIdx.x;
   const int64_t p = q_pos[row];
-  if (p < 0 || p >= ld) {
-    if (tid == 0) report(status, DSA_DEV_BAD_QPOS);
-    for (int j = tid; j < k; j += RNT) out[j] = -1;
-    return;
+  const bool bad = p < 0 || p >= ld;
+  int32_t* out = idx + row * (int64_t)k;
+  const float* s;  // the scores this CTA selects from
+  int vis;         // how many of them
+  int64_t wbase = 0;
+  int64_t first = 0;  // ROW_SLICE: the slice's first position
+  if (MODE == ROW_SLICE) {
+    first = (int64_t)(blockIdx.x % nslices) * RMAXV;
+    const int64_t len = bad ? 0 : (p + 1 - first < 0 ? 0 : (p + 1 - first < RMAXV ? p + 1 - first : RMAXV));
+    s = scores + row * ld + first;
+    vis = (int)len;
+    wbase = (int64_t)blockIdx.x * k;
+    if (vis <= k) {  // the whole slice (maybe empty), then padding
+      for (int j = tid; j < k; j += RNT) {
+        ws_pos[wbase + j] = j < vis ? (int32_t)(first + j) : -1;
+        ws_score[wbase + j] = j < vis ? s[j] : __uint_as_float(PAD_SCORE_BITS);
+      }
+      return;
+    }
+  } else {
+    if (MODE == ROW_MERGE) asm volatile("griddepcontrol.wait;" ::: "memory");  // the slices' blocks
+    if (bad) {
+      if (tid == 0) report(status, DSA_DEV_BAD_QPOS);
+      for (int j = tid; j < k; j += RNT) out[j] = -1;
+      return;
+    }
+    if (p + 1 <= k) {
+      for (int j = tid; j < k; j += RNT) out[j] = j < p + 1 ? j : -1;
+      return;
+    }
+    if (MODE == ROW_MERGE) {
+      wbase = row * (int64_t)nslices * k;
+      s = ws_score + wbase;
+      vis = nslices * k;  // <= RMAXV
+    } else {
+      s = scores + row * ld;
+      vis = (int)(p + 1);  // <= ld <= RMAXV
+    }
   }
-  const int vis = (int)(p + 1);  // <= ld <= RMAXV
-  if (vis <= k) {
-    for (int j = tid; j < k; j += RNT) out[j] = j < vis ? j : -1;
-    return;
-  }
-  const float* s = scores + row * ld;
+  // output slot o gets the element at offset q of s
+  auto emit = [&](uint32_t o, int32_t q) {
+    if (MODE == ROW_PLAIN) {
+      out[o] = q;
+    } else if (MODE == ROW_SLICE) {
+      ws_pos[wbase + o] = (int32_t)(first + q);
+      ws_score[wbase + o] = s[q];
+    } else {
+      out[o] = ws_pos[wbase + q];
+    }
+  };
   const int head0 = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(s) & 15u)) & 15u) >> 2);
   const int h0 = head0 < vis ? head0 : vis;  // positions before the first 16-byte boundary
   const int nv4 = (vis - h0) >> 2;           // whole float4s after them
@@ -508,8 +563,8 @@ __global__ void __launch_bounds__(RNT, 2)
   };
 
   // ---- 0. loads in this order: a 1/16 sample (the first 8 of every 128
-  // positions), the whole row into L2 (eight 16-byte-aligned pieces inside
-  // it), the first half-batch of the stream ----
+  // positions), then the whole row into L2 (eight 16-byte-aligned pieces
+  // inside it) ----
   const bool sampled = vis > RALL;
   const int blk = tid * SAMPLE_BLOCK;  // one sample block per thread covers a row
   float sv[SAMPLE_RUN];
@@ -602,7 +657,7 @@ __global__ void __launch_bounds__(RNT, 2)
   }
   if (full || total < (uint32_t)k) {
     // the sample misled: exact selection over the row in global memory
-    select_exact<true>(s, nullptr, nullptr, vis, (uint32_t)k, out, hist, warp_buf, sel);
+    select_exact<true>(s, nullptr, nullptr, vis, (uint32_t)k, emit, hist, warp_buf, sel);
     return;
   }
 
@@ -694,7 +749,7 @@ __global__ void __launch_bounds__(RNT, 2)
     while (a && o < (uint32_t)k) {
       const int b = __ffs(a) - 1;
       a &= a - 1u;
-      out[o++] = (tid * WPT + j) * 32 + b;
+      emit(o++, (tid * WPT + j) * 32 + b);
     }
   }
 }
@@ -722,13 +777,55 @@ int topk_cluster_size(int32_t num_q, int64_t ld, int num_sms) {
   return c;
 }
 
+size_t topk_workspace_bytes(int32_t num_q, int64_t ld, int32_t k) {
+  if (num_q <= 0 || k <= 0 || ld <= RMAXV) return 0;
+  const int64_t slices = (ld + RMAXV - 1) / RMAXV;
+  if (slices * k > RMAXV) return 0;  // the union would not fit one CTA: the cluster kernel runs
+  return (size_t)num_q * (size_t)slices * (size_t)k * (sizeof(float) + sizeof(int32_t));
+}
+
 cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
-                        int32_t* idx, int32_t* dev_status, cudaStream_t stream) {
+                        int32_t* idx, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        cudaStream_t stream) {
   if (num_q == 0) return cudaSuccess;
   if (ld <= RMAXV) {
-    cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RSMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(topk_row_kernel<ROW_PLAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RSMEM);
     if (e != cudaSuccess) return e;
-    topk_row_kernel<<<(unsigned)num_q, RNT, RSMEM, stream>>>(scores, ld, q_pos, k, idx, dev_status);
+    topk_row_kernel<ROW_PLAIN><<<(unsigned)num_q, RNT, RSMEM, stream>>>(scores, ld, q_pos, k, idx, dev_status,
+                                                                        nullptr, nullptr, 1);
+    return cudaGetLastError();
+  }
+  const size_t need = topk_workspace_bytes(num_q, ld, k);
+  if (need > 0 && workspace != nullptr && workspace_bytes >= need) {
+    // slices of RMAXV positions, then one merge per row (a programmatic
+    // dependent launch that waits for the slices' blocks)
+    const int slices = (int)((ld + RMAXV - 1) / RMAXV);
+    float* ws_score = static_cast<float*>(workspace);
+    int32_t* ws_pos = reinterpret_cast<int32_t*>(ws_score + (size_t)num_q * slices * k);
+    cudaError_t e =
+        cudaFuncSetAttribute(topk_row_kernel<ROW_SLICE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RSMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_row_kernel<ROW_MERGE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RSMEM);
+    if (e != cudaSuccess) return e;
+    topk_row_kernel<ROW_SLICE><<<(unsigned)num_q * slices, RNT, RSMEM, stream>>>(scores, ld, q_pos, k, idx,
+                                                                                 dev_status, ws_score, ws_pos,
+                                                                                 slices);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)num_q);
+    cfg.blockDim = dim3(RNT);
+    cfg.dynamicSmemBytes = RSMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, topk_row_kernel<ROW_MERGE>, scores, ld, q_pos, k, idx, dev_status, ws_score,
+                           ws_pos, slices);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
   const int sms = device_sm_count();

@@ -94,16 +94,23 @@ DSA_API int32_t dsa_version(void);
  *   scores     fp32 [num_q, ld_scores], row stride ld_scores elements.
  *   q_pos      int32 [num_q]; q_pos[i] must lie in [0, ld_scores).
  *   idx        int32 [num_q, k] output.
- *   workspace  device scratch of at least dsa_topk_workspace_size() bytes
- *              (may be NULL when that size is 0).
+ *   workspace  optional device scratch (caller-owned, no alignment beyond
+ *              4 bytes).  Rows longer than 65,536 positions use it when
+ *              dsa_topk_workspace_size() > 0: each 65,536-position slice
+ *              writes its own top k there and a second pass merges them.
+ *              NULL with workspace_bytes = 0 selects the slower in-place
+ *              path instead; both give the same indices.
  * Errors: num_q < 0, k <= 0, ld_scores <= 0, null pointers -> INVALID_ARG;
+ * 0 < workspace_bytes < dsa_topk_workspace_size() -> WORKSPACE_TOO_SMALL;
  * q_pos out of range -> dev bit DSA_DEV_BAD_QPOS and a row of -1.
  */
 DSA_API dsa_status dsa_topk_select(const float* scores, int64_t ld_scores, const int32_t* q_pos, int32_t num_q,
                            int32_t k, int32_t* idx, void* workspace, size_t workspace_bytes,
                            int32_t* dev_status, void* stream);
 
-/* Scratch bytes dsa_topk_select needs for these sizes. */
+/* Workspace bytes dsa_topk_select can use for these sizes: num_q x slices x k x 8
+ * when ld_scores > 65,536 and slices x k <= 65,536 (slices = ceil(ld_scores /
+ * 65,536)), else 0. */
 DSA_API size_t dsa_topk_workspace_size(int32_t num_q, int64_t ld_scores, int32_t k);
 
 /*

@@ -114,6 +114,10 @@ def test_fwd_argument_checks(lib, over, expect):
     ((FAKE, 100, FAKE, 4, 8, None, None, 0, None, None), 1),
     ((FAKE, 100, FAKE, -1, 8, FAKE, None, 0, None, None), 1),
     ((FAKE, 100, FAKE, 0, 8, FAKE, None, 0, None, None), 0),
+    # rows longer than 65,536 positions: a partial workspace is an error, a
+    # sized one without a pointer too (both checked before any launch)
+    ((FAKE, 1 << 20, FAKE, 16, 2048, FAKE, FAKE, 100, None, None), 3),
+    ((FAKE, 1 << 20, FAKE, 16, 2048, FAKE, None, 16 * 16 * 2048 * 8, None, None), 1),
 ])
 def test_topk_argument_checks(lib, args, expect):
     assert lib.dsa_topk_select(*args) == expect
@@ -130,6 +134,15 @@ def test_topk_argument_checks(lib, args, expect):
 ])
 def test_combine_argument_checks(lib, args, expect):
     assert lib.dsa_combine(*args) == expect
+
+
+def test_topk_workspace_size(lib):
+    # (score, position) blocks of k per 65,536-position slice of every row
+    assert dsa.topk_workspace_size(16, 1 << 20, 2048) == 16 * 16 * 2048 * 8
+    assert dsa.topk_workspace_size(3, 70001, 100) == 3 * 2 * 100 * 8
+    assert dsa.topk_workspace_size(128, 65536, 2048) == 0        # one slice: no merge needed
+    assert dsa.topk_workspace_size(4, 70001, 33000) == 0         # the union would exceed a row
+    assert dsa.topk_workspace_size(0, 1 << 20, 2048) == 0
 
 
 def test_workspace_size(lib):

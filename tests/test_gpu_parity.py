@@ -112,6 +112,9 @@ def test_path_matches_oracle(w, nsample):
     assert_close(host(out.float())[rows], host(lse)[rows], ref_out, ref_lse, w.name)
 
 
+NO_WORKSPACE = torch.empty(0, dtype=torch.uint8)  # selects the in-place path for rows > 65,536
+
+
 @pytest.mark.parametrize("w", [wl.DECODE_64K, wl.VERIFY_64K, wl.CTX_1M], ids=lambda w: w.name)
 def test_topk_whole_index_array_bit_exact(w):
     inp = inputs(w)
@@ -119,6 +122,10 @@ def test_topk_whole_index_array_bit_exact(w):
     torch.cuda.synchronize()
     ref = oracle.topk(host(inp.scores), host(inp.q_pos), w.k)
     assert np.array_equal(host(idx), ref)
+    if inp.scores.shape[1] > 65536:  # the 1M rows: sliced path above, in-place cluster path here
+        idx2 = dsa.topk_select(inp.scores, inp.q_pos, w.k, workspace=NO_WORKSPACE)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(idx2), ref)
 
 
 def test_topk_prefill_rows_bit_exact_sampled():
@@ -321,13 +328,19 @@ def test_topk_sampling_fallbacks(ld):
     rows.append(r4)
     scores = np.stack(rows)
     q_pos = np.array([ld - 1, ld - 1, ld - 100, ld - 7, ld - 1, ld - 3], dtype=np.int32)
+    ref = oracle.topk(scores, q_pos, k)
     got = dsa.topk_select(torch.tensor(scores, device="cuda"), torch.tensor(q_pos, device="cuda"), k)
-    assert np.array_equal(host(got), oracle.topk(scores, q_pos, k))
-    # the same rows in a batch big enough to use multi-CTA clusters
+    assert np.array_equal(host(got), ref)
+    # rows longer than 65,536: the in-place cluster path too, alone and in a
+    # batch big enough to use multi-CTA clusters
     big = np.concatenate([scores] * 2)
     qp = np.concatenate([q_pos] * 2)
-    got = dsa.topk_select(torch.tensor(big, device="cuda"), torch.tensor(qp, device="cuda"), k)
-    assert np.array_equal(host(got), oracle.topk(big, qp, k))
+    for ws in ((None, NO_WORKSPACE) if ld > 65536 else (None,)):
+        got = dsa.topk_select(torch.tensor(scores, device="cuda"), torch.tensor(q_pos, device="cuda"), k,
+                              workspace=ws)
+        assert np.array_equal(host(got), ref)
+        got = dsa.topk_select(torch.tensor(big, device="cuda"), torch.tensor(qp, device="cuda"), k, workspace=ws)
+        assert np.array_equal(host(got), oracle.topk(big, qp, k))
 
 
 def test_dcp_path_with_library_kernels_in_a_group_of_one():
@@ -408,9 +421,31 @@ def test_topk_edges_bit_exact(ld):
     v = torch.sort(sc[14, :vis], descending=True).values[k - 10]
     sc[14, torch.randperm(vis, generator=g)[:40]] = v
     scores = sc.cuda()
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    idx = dsa.topk_select(scores, torch.from_numpy(q_pos).cuda(), k, dev_status=status)
-    torch.cuda.synchronize()
-    assert int(status.item()) == 0
     ref = oracle.topk(sc.numpy(), q_pos, k)
-    assert np.array_equal(host(idx), ref)
+    for ws in ((None, NO_WORKSPACE) if ld > 65536 else (None,)):  # sliced and in-place paths
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        idx = dsa.topk_select(scores, torch.from_numpy(q_pos).cuda(), k, dev_status=status, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.array_equal(host(idx), ref)
+
+
+def test_topk_long_rows_paths_and_large_k():
+    """Rows longer than 65,536 positions: the sliced path with slices shorter
+    than k, empty slices and a bad q_pos row; and k so large that the union of
+    the slices' blocks exceeds a row, which takes the in-place path by itself."""
+    g = torch.Generator().manual_seed(53)
+    ld = 200003
+    sc = torch.randn((6, ld), generator=g)
+    sc[2, 131072:] += 3.0                       # the last slices hold the large scores
+    q_pos = np.array([ld - 1, 65536, 131071, 70000, 200000, ld + 5], dtype=np.int32)
+    for k in (100, 2048, 20000):
+        qp = q_pos.copy()
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        idx = dsa.topk_select(sc.cuda(), torch.from_numpy(qp).cuda(), k, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 1  # DSA_DEV_BAD_QPOS from the last row
+        got = host(idx)
+        assert (got[5] == -1).all()
+        assert np.array_equal(got[:5], oracle.topk(sc.numpy()[:5], qp[:5], k))
+    assert dsa.topk_workspace_size(6, ld, 20000) == 0  # 4 slices x 20000 > 65,536
