@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(RNT, 2)
                     int32_t* __restrict__ idx, int32_t* status, float* __restrict__ ws_score,
                     int32_t* __restrict__ ws_pos, int nslices) {
   extern __shared__ __align__(16) uint32_t rsm[];
-  uint32_t* ckey = rsm;                                              // [RLCAP] candidate keys
+  uint32_t* ckey = rsm;                                              // [RLCAP] candidate scores, then keys
   uint32_t* hist = ckey + RLCAP;                                     // [HBINS]
   uint32_t* above_bm = hist + HBINS;                                 // [RWORDS] keys above the threshold
   uint32_t* equal_bm = above_bm + RWORDS;                            // [RWORDS] keys equal to it
@@ -603,15 +603,23 @@ __global__ void __launch_bounds__(RNT, 2)
   }
 
   // ---- 2. one streaming pass; each warp lists its candidates ----
+  // The screen is a float compare: for every score that is not a NaN,
+  // key(x) >= T_lo exactly when x >= f_lo, f_lo being the number whose key is
+  // T_lo (-inf when T_lo lies below the key of -inf; a NaN, which nothing
+  // passes, when it lies above the key of +inf).  The list keeps the scores'
+  // bits; keys are formed only for the candidates, after the stream.
+  const uint32_t lo_bits = t_lo >= 0x80000000u ? (t_lo & 0x7fffffffu) : ~t_lo;
+  const float f_lo = t_lo < 0x80000000u && lo_bits > 0xff800000u ? -INFINITY : __uint_as_float(lo_bits);
   uint32_t wcnt = 0;  // the same in every lane of the warp
   uint32_t* wkey = ckey + warp * RWCAP;
   uint16_t* wpos = cpos + warp * RWCAP;
-  auto push = [&](bool cand, uint32_t key, int pos) {
+  const uint32_t lanes_below = (1u << lane) - 1u;
+  auto push = [&](bool cand, float x, int pos) {
     const uint32_t b = __ballot_sync(0xffffffffu, cand);
     if (b) {
-      const uint32_t r = wcnt + __popc(b & ((1u << lane) - 1u));
+      const uint32_t r = wcnt + __popc(b & lanes_below);
       if (cand && r < (uint32_t)RWCAP) {
-        wkey[r] = key;
+        wkey[r] = __float_as_uint(x);
         wpos[r] = (uint16_t)pos;
       }
       wcnt += __popc(b);
@@ -623,12 +631,10 @@ __global__ void __launch_bounds__(RNT, 2)
       const int f = base + d * RNT + tid;
       const bool ok = f < nv4;
       const int e = h0 + 4 * f;
-      const uint32_t k0 = score_key(v[d].x), k1 = score_key(v[d].y);
-      const uint32_t k2 = score_key(v[d].z), k3 = score_key(v[d].w);
-      push(ok && k0 >= t_lo, k0, e);
-      push(ok && k1 >= t_lo, k1, e + 1);
-      push(ok && k2 >= t_lo, k2, e + 2);
-      push(ok && k3 >= t_lo, k3, e + 3);
+      push(ok && v[d].x >= f_lo, v[d].x, e);
+      push(ok && v[d].y >= f_lo, v[d].y, e + 1);
+      push(ok && v[d].z >= f_lo, v[d].z, e + 2);
+      push(ok && v[d].w >= f_lo, v[d].w, e + 3);
     }
   };
   // the loads of one half-batch are in flight while the other is screened
@@ -643,8 +649,8 @@ __global__ void __launch_bounds__(RNT, 2)
   if (warp == 0) {  // the unaligned head (lanes 0-2) and tail (lanes 4-6)
     const int nt = vis - h0 - 4 * nv4;
     const int pe = lane < h0 ? lane : (lane >= 4 && lane - 4 < nt ? h0 + 4 * nv4 + lane - 4 : -1);
-    const uint32_t key = pe >= 0 ? score_key(__ldg(s + pe)) : 0u;
-    push(pe >= 0 && key >= t_lo, key, pe);
+    const float x = pe >= 0 ? __ldg(s + pe) : 0.f;
+    push(pe >= 0 && x >= f_lo, x, pe);
   }
   if (lane == 0) wcount[warp] = wcnt;
   __syncthreads();
@@ -671,7 +677,8 @@ __global__ void __launch_bounds__(RNT, 2)
 #pragma unroll
   for (int w = 0; w < RWARPS; ++w) {
     if ((have >> w) & 1u) {
-      const uint32_t key = ckey[w * RWCAP + tid];
+      const uint32_t key = score_key(__uint_as_float(ckey[w * RWCAP + tid]));
+      ckey[w * RWCAP + tid] = key;  // from here on the list holds keys
       lo = min(lo, key);
       hi = max(hi, key);
     }
