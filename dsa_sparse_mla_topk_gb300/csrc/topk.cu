@@ -2,25 +2,25 @@
 //
 // "Accelerating GLM-5.3-Flash on H200", section 3 "Larger KV tiles for DSA
 // Partial": the indexer's scores pick the KV positions the Partial step
-// attends to.  This kernel makes the pick exact and deterministic: positions
+// attends to.  These kernels make the pick exact and deterministic: positions
 // are ranked by (score descending, position ascending), -0.0 == +0.0, and
 // the chosen ones are written in ascending position order, -1 padded.
 //
-// Every fp32 score maps to an order-preserving 32-bit key.  A row is handled
-// by a thread-block cluster of C CTAs, each owning a contiguous slice of the
-// visible positions:
-//   1. each CTA histograms the top 12 key bits of a 1/16 sample of its slice;
-//      the histograms are summed over the cluster (distributed shared memory)
-//      and give a lower threshold T_lo that, with a wide safety margin, lies
-//      below the k-th largest key;
-//   2. one streaming pass collects every key >= T_lo with its position, in
-//      position order (warp ballots + a scan of warp counts);
-//   3. CTA 0 gathers the candidates of the cluster, finds the exact key T of
-//      the k-th largest entry by radix select over the candidates, and writes
-//      the keys above T plus the lowest-positioned entries equal to T.
-// If the sample misleads (fewer than k candidates, or more than fit), CTA 0
-// falls back to an exact multi-pass radix select over the whole row in
-// global memory, so the result never depends on the score distribution.
+// Every fp32 score maps to an order-preserving 32-bit key.  Two kernels:
+//   topk_row_kernel      rows of up to 65,536 positions, one CTA per row; longer
+//                        rows one CTA per 65,536-position slice plus a merge of
+//                        the slices' top-k blocks (needs the caller's workspace);
+//   topk_cluster_kernel  long rows without a workspace: a thread-block
+//                        cluster of C CTAs per row, each owning a contiguous
+//                        slice of the visible positions.
+// Both follow the same plan: a 1/16 sample places a lower threshold T_lo that,
+// with a wide margin, lies below the k-th largest key; one streaming pass
+// collects the keys >= T_lo with their positions; an exact radix select over
+// those candidates finds the k-th largest key T; the keys above T and the
+// lowest-positioned keys equal to T are written.  If the sample misleads
+// (fewer than k candidates, or more than fit), the CTA falls back to an exact
+// multi-pass radix select over the row in global memory, so the result never
+// depends on the score distribution.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -188,7 +188,7 @@ __device__ void select_exact(const float* row_scores, const uint32_t* keys, cons
 
 template <int C>
 struct TopkSmem {
-  // candidates one CTA collects; sized so that two 1024-thread CTAs fit on an SM
+  // candidates one CTA collects; sized so that two CTAs fit on an SM
   static constexpr int LCAP = C == 1 ? MCAP : 3072;
   static constexpr size_t bytes = sizeof(uint32_t) * HBINS + (sizeof(uint32_t) + sizeof(int32_t)) * LCAP +
                                   (C > 1 ? (sizeof(uint32_t) + sizeof(int32_t)) * MCAP : 0);
@@ -389,13 +389,14 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
 // Rows of up to 65,536 visible positions: one CTA of 512 threads per row,
 // two CTAs per SM (80 KB of shared memory each), so that one CTA streams
 // while the other selects.
-//   0. An L2 bulk prefetch of the whole row is issued first.
-//   1. A 1/16 sample (the first 8 of every 128 positions) places a lower
-//      12-bit threshold T_lo as in the cluster kernel.
-//   2. One streaming pass screens every key against T_lo in registers.  Each
-//      warp appends its candidates (full key, position) to its own segment
-//      of a shared-memory list through ballots: no atomics, no block-wide
-//      synchronisation.
+//   0. The loads of a 1/16 sample (the first 8 of every 128 positions) are
+//      issued first, then an L2 bulk prefetch of the whole row.
+//   1. The sample places a lower 12-bit threshold T_lo as in the cluster
+//      kernel.
+//   2. One streaming pass screens every score against T_lo with one float
+//      compare.  Each warp appends its candidates (score bits, position) to
+//      its own segment of a shared-memory list through ballots: no atomics,
+//      no block-wide synchronisation.
 //   3. The k-th largest candidate key is found exactly by radix passes over
 //      (key - min key), up to 11 bits each, from the highest significant bit.
 //   4. The keys above it and the keys equal to it are marked in two position
