@@ -382,3 +382,41 @@ def test_kv_write_scatters_through_the_block_table():
     st = oracle.kv_write(x[:1].view(torch.int16).numpy(), np.zeros(1, np.int32), np.zeros(1, np.int32), bad_page,
                          kv, sc, page_size=P)
     assert st == oracle.BAD_PAGE
+
+
+def test_topk_of_slice_topks_is_the_row_topk():
+    """The sliced top-k for long rows keeps each fixed-size slice's own top k
+    (score, position) in position order, concatenates the blocks in slice
+    order, and takes the top k of that union; union order is position order,
+    so the lower-index tie rule there is the lower-position rule.  Checked
+    with the oracle alone: slices shorter than k, empty slices, and exact
+    ties across slice boundaries must give the row's own top k."""
+    rng = np.random.default_rng(17)
+    slice_len, k = 96, 40
+    ld = 5 * slice_len + 17
+    scores = rng.standard_normal((6, ld)).astype(np.float32)
+    scores[1] = rng.integers(0, 3, ld).astype(np.float32)          # heavy ties everywhere
+    scores[2, 90:110] = 7.0                                        # a tie run across a slice edge
+    scores[3, slice_len * 3:] += 5.0                               # the top k all in late slices
+    q_pos = np.array([ld - 1, ld - 1, ld - 1, ld - 1, slice_len + 3, 2 * slice_len - 1], dtype=np.int32)
+    want = oracle.topk(scores, q_pos, k)
+    nsl = (ld + slice_len - 1) // slice_len
+    for r in range(scores.shape[0]):
+        vis = int(q_pos[r]) + 1
+        blk_score, blk_pos = [], []
+        for sl in range(nsl):
+            lo = sl * slice_len
+            n = max(0, min(vis - lo, slice_len))
+            if n == 0:
+                continue
+            part = scores[r:r + 1, lo:lo + n]
+            sel = oracle.topk(part, np.array([n - 1], dtype=np.int32), k)[0]
+            sel = sel[sel >= 0]
+            blk_score.append(part[0, sel])
+            blk_pos.append(lo + sel)
+        union_s = np.concatenate(blk_score)[None, :]
+        union_p = np.concatenate(blk_pos)
+        assert (np.diff(union_p) > 0).all()                        # union order is position order
+        pick = oracle.topk(union_s, np.array([union_s.shape[1] - 1], dtype=np.int32), k)[0]
+        got = np.where(pick >= 0, union_p[np.maximum(pick, 0)], -1)
+        assert np.array_equal(got, want[r]), r
