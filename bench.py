@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--cpu-sample", type=int, default=64, help="query tokens the oracle baseline times")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--copy-streams", type=int, default=2,
+                    help="copy streams of the end-to-end leg; q and scores are split over them by rows")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--kv-write-rows", type=int, default=32768,
                     help="rows of the separate KV-write measurement (0 = skip)")
@@ -381,8 +383,11 @@ def bench_ours(args):
         lse_h = [torch.empty(bufs["lse"].shape, dtype=bufs["lse"].dtype).pin_memory() for _ in range(NB)]
         h2d = sum(t.numel() * t.element_size() for t in pin.values())
         d2h = out_h[0].numel() * out_h[0].element_size() + lse_h[0].numel() * lse_h[0].element_size()
-        cs = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-        half = inp.scores.shape[0] // 2
+        cs = [torch.cuda.Stream(dev) for _ in range(max(1, args.copy_streams))]
+
+        def rows_of(t, c):  # stream c's share of tensor t's rows
+            n = t.shape[0]
+            return slice(n * c // len(cs), n * (c + 1) // len(cs))
 
         def ev():
             return torch.cuda.Event(enable_timing=True)
@@ -398,19 +403,18 @@ def bench_ours(args):
                     if i >= NB:
                         stream_c.wait_event(comp_done[i - NB])  # that step's compute has read these inputs
                     with torch.cuda.stream(stream_c):
-                        if c == 0:
-                            for n in names:
-                                if n == "scores":
-                                    dsts[b][n][:half].copy_(pin[n][:half], non_blocking=True)
-                                else:
-                                    dsts[b][n].copy_(pin[n], non_blocking=True)
-                        else:
-                            dsts[b]["scores"][half:].copy_(pin["scores"][half:], non_blocking=True)
+                        for n in names:
+                            if n in ("q", "scores"):
+                                r = rows_of(pin[n], c)
+                                dsts[b][n][r].copy_(pin[n][r], non_blocking=True)
+                            elif c == 0:
+                                dsts[b][n].copy_(pin[n], non_blocking=True)
                     h2d_done[i][c].record(stream_c)
 
             start, end = ev(), ev()
             start.record(cs[0])
-            cs[1].wait_event(start)
+            for stream_c in cs[1:]:
+                stream_c.wait_event(start)
             issue_h2d(0)
             for i in range(nsteps):
                 b = i % NB
@@ -447,7 +451,8 @@ def bench_ours(args):
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
                "note": "KV cache resident in HBM; every step copies its inputs (q, scores, q_pos, q_req, block "
                        "table) from pinned host memory and reads out + lse back inside the timed region; step "
-                       "i+1's input copies overlap step i's compute (double buffers, two copy streams); L2 "
+                       "i+1's input copies overlap step i's compute (double buffers, copies split over "
+                       f"{len(cs)} copy streams); L2 "
                        "flushed before every step's compute"}
     torch.cuda.synchronize(dev)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
