@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--cpu-sample", type=int, default=64, help="query tokens the oracle baseline times")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="also write the raw clock samples to this CSV ({rank} is replaced by the rank)")
     ap.add_argument("--copy-streams", type=int, default=2,
                     help="copy streams of the end-to-end leg; q and scores are split over them by rows")
     ap.add_argument("--no-clocks", action="store_true")
@@ -344,8 +346,7 @@ def bench_ours(args):
         torch.cuda.synchronize(dev)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    clock_path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if os.path.isdir(
-        os.path.join(ROOT, "gpurun_out")) else None
+    clock_path = args.clocks_csv.format(rank=rank) if args.clocks_csv else None
     sampler = ClockSampler(gpu_uuid(torch, dev), clock_path) if not args.no_clocks else None
     if sampler:
         sampler.__enter__()
