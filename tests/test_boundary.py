@@ -176,3 +176,22 @@ def _kvw(lib, **over):
 def test_kv_write_argument_checks(lib, over, expect):
     """Every case returns before any CUDA call (fake device pointers)."""
     assert _kvw(lib, **over) == expect
+
+
+def test_pick_num_splits_rule(lib):
+    """The split rule on a 152-SM GB300 (no device needed): no split once the
+    query tokens fill the SMs; the 16-token 1M-context workload splits 8 ways;
+    never more splits than 64-row tiles; unsupported shapes get 1."""
+    sms = 152
+    assert dsa.pick_num_splits(128, 64, 512, 64, 2048, sms) == 1          # decode
+    assert dsa.pick_num_splits(1024, 64, 512, 64, 2048, sms) == 1         # verify
+    assert dsa.pick_num_splits(32768, 64, 512, 64, 2048, sms) == 1        # prefill
+    assert dsa.pick_num_splits(16, 64, 512, 64, 2048, sms) == 8           # 1M context
+    for nq in (1, 2, 5, 17, 75, 151, 152, 400):
+        s = dsa.pick_num_splits(nq, 64, 512, 64, 2048, sms)
+        assert 1 <= s <= 32                                               # 2048 / 64 tiles
+        if nq >= sms:
+            assert s == 1
+    assert dsa.pick_num_splits(4, 64, 512, 64, 100, sms) <= 2             # 100 rows: 2 tiles
+    assert dsa.pick_num_splits(4, 32, 512, 64, 2048, sms) == 1            # unsupported heads
+    assert dsa.pick_num_splits(0, 64, 512, 64, 2048, sms) == 1
