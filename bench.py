@@ -502,7 +502,7 @@ def bench_ours(args):
         kvw["frac"] = kvw["achieved_gbs"] / peaks["hbm_gbs"]
     fwd_ms = statistics.mean(t_fwd)
     src = os.path.join(ROOT, "dsa_sparse_mla_topk_gb300", "csrc",
-                       "mla_tc.cu" if w.heads == 64 and os.environ.get("DSA_FORCE_SIMT") != "1" else "mla_simt.cu")
+                       "mla_tc.cu" if w.heads == 64 else "mla_simt.cu")
     sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
     tr = TRAFFIC_BY_SOURCE.get(sha)
     traffic = None

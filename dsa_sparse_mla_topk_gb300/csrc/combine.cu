@@ -15,22 +15,29 @@ namespace dsa {
 namespace {
 
 constexpr int kCombineThreads = 256;
-constexpr int kChunk = 4 * kCombineThreads;  // floats of one query's H x d_v block per CTA
+constexpr int kMaxChunk = 4 * kCombineThreads;  // floats of one query's H x d_v block per CTA
 constexpr int kMaxSplits = 64;
 constexpr int kMaxChunkHeads = 32;
 
-// CTA (i, c): floats [c kChunk, (c + 1) kChunk) of query i's H x d_v result.
+// Floats per CTA for rows of d_v floats: a chunk of c floats touches at most
+// c / d_v + 2 heads, which must fit the kMaxChunkHeads weight columns.
+int chunk_floats(int dv) {
+  const int c = (kMaxChunkHeads - 2) * dv;
+  return c < kMaxChunk ? (c & ~3) : kMaxChunk;
+}
+
+// CTA (i, c): floats [c chunk, (c + 1) chunk) of query i's H x d_v result.
 // First the per-(split, head) weights of the heads that chunk touches, then
 // one float4 per thread, all splits' loads in flight together.
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int S, int num_q, int H,
-                   int dv, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+                   int dv, int chunk, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   __shared__ float w[kMaxSplits * kMaxChunkHeads];
   const int i = blockIdx.x;
-  const int64_t e0 = (int64_t)blockIdx.y * kChunk;
+  const int64_t e0 = (int64_t)blockIdx.y * chunk;
   const int64_t n = (int64_t)H * dv;
   const int h0 = (int)(e0 / dv);
-  const int h1 = (int)(min(e0 + kChunk, n) - 1) / dv;
+  const int h1 = (int)(min(e0 + chunk, n) - 1) / dv;
   for (int t = threadIdx.x; t <= h1 - h0; t += blockDim.x) {
     const int h = h0 + t;
     float m = -INFINITY;
@@ -50,7 +57,7 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
   __syncthreads();
   const int64_t e = e0 / 4 + threadIdx.x;  // float4 index within the query
-  if (e * 4 >= n) return;
+  if (4 * (int)threadIdx.x >= chunk || e * 4 >= n) return;
   const int t = (int)(e * 4 / dv) - h0;
   const int64_t stride_s = (int64_t)num_q * H * dv / 4;
   const float4* base = reinterpret_cast<const float4*>(o_part + (int64_t)i * H * dv) + e;
@@ -87,12 +94,11 @@ __global__ void __launch_bounds__(kCombineThreads)
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t num_q,
                            int32_t heads, int32_t d_v, void* out, float* lse, cudaStream_t stream) {
   if (num_q == 0) return cudaSuccess;
-  // a chunk touches at most kChunk / d_v + 1 heads; d_v is a multiple of 4
-  if (num_splits > kMaxSplits || d_v <= 0 || d_v % 4 != 0 || kChunk / d_v + 2 > kMaxChunkHeads)
-    return cudaErrorInvalidValue;
+  if (num_splits > kMaxSplits || d_v <= 0 || d_v % 4 != 0) return cudaErrorInvalidValue;
+  const int chunk = chunk_floats(d_v);
   const int64_t n = (int64_t)heads * d_v;
-  const dim3 grid(num_q, (unsigned)((n + kChunk - 1) / kChunk));
-  combine_kernel<<<grid, kCombineThreads, 0, stream>>>(o_part, lse_part, num_splits, num_q, heads, d_v,
+  const dim3 grid(num_q, (unsigned)((n + chunk - 1) / chunk));
+  combine_kernel<<<grid, kCombineThreads, 0, stream>>>(o_part, lse_part, num_splits, num_q, heads, d_v, chunk,
                                                        static_cast<__nv_bfloat16*>(out), lse);
   return cudaGetLastError();
 }

@@ -1,7 +1,6 @@
 // C ABI of the library: argument checks, planning helpers and launches.
 #include <cuda_runtime.h>
 #include <math.h>
-#include <stdlib.h>
 
 #include "dsa.h"
 #include "internal.cuh"
@@ -16,12 +15,9 @@ bool supported_shape(int32_t h, int32_t dl, int32_t dr) {
 
 dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
-// The 64-head shape runs on the tensor cores unless DSA_FORCE_SIMT=1 asks for
-// the CUDA-core kernel (used to cross-check the two on the GPU).
-bool use_tensor_cores(int32_t h, int32_t dl, int32_t dr) {
-  const char* force = getenv("DSA_FORCE_SIMT");
-  return h == 64 && dl == 512 && dr == 64 && !(force && force[0] == '1');
-}
+// The 64-head shape runs on the tensor cores, the 16-head shape on the CUDA
+// cores; nothing else changes that choice.
+bool use_tensor_cores(int32_t h, int32_t dl, int32_t dr) { return h == 64 && dl == 512 && dr == 64; }
 
 }  // namespace
 
@@ -113,6 +109,61 @@ dsa_status dsa_topk_select(const float* scores, int64_t ld_scores, const int32_t
                                     dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace {
+
+// Argument checks shared by the attention entry points; fills `a` when they pass.
+dsa_status check_mla_args(const void* q, const uint8_t* kv, const float* kv_scale, int64_t num_pages,
+                          const int32_t* block_table, int32_t num_req, int32_t bt_stride, const int32_t* q_req,
+                          const int32_t* idx, int32_t num_q, int32_t num_heads, int32_t d_latent, int32_t d_rope,
+                          int32_t page_size, int32_t k, float softmax_scale, int32_t num_splits, void* out,
+                          float* lse, float* o_part, float* lse_part, size_t ws_need, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, dsa::MlaArgs* a) {
+  if (num_q < 0 || k <= 0 || page_size <= 0 || num_pages <= 0 || num_req <= 0 || bt_stride <= 0)
+    return DSA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 64 || !isfinite(softmax_scale)) return DSA_ERR_INVALID_ARG;
+  if (!supported_shape(num_heads, d_latent, d_rope)) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (num_pages > (int64_t)INT32_MAX / page_size) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (num_q == 0) return DSA_OK;
+  if (workspace_bytes < ws_need) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 7u))) return DSA_ERR_INVALID_ARG;
+  if (!q || !kv || !kv_scale || !block_table || !q_req || !idx) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
+  if (num_splits == 1) {
+    if (!out || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+  } else {
+    if (!o_part || !lse_part || !aligned16(o_part)) return DSA_ERR_INVALID_ARG;
+  }
+  a->q = q;
+  a->kv = kv;
+  a->kv_scale = kv_scale;
+  a->num_pages = num_pages;
+  a->block_table = block_table;
+  a->num_req = num_req;
+  a->bt_stride = bt_stride;
+  a->q_req = q_req;
+  a->idx = idx;
+  a->num_q = num_q;
+  a->heads = num_heads;
+  a->d_latent = d_latent;
+  a->d_rope = d_rope;
+  a->page_size = page_size;
+  a->k = k;
+  a->softmax_scale = softmax_scale;
+  a->num_splits = num_splits;
+  a->out = out;
+  a->lse = lse;
+  a->o_part = o_part;
+  a->lse_part = lse_part;
+  a->dev_status = dev_status;
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_scale, int64_t num_pages,
                               const int32_t* block_table, int32_t num_req, int32_t bt_stride,
                               const int32_t* q_req, const int32_t* idx, int32_t num_q, int32_t num_heads,
@@ -120,47 +171,35 @@ dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_
                               float softmax_scale, int32_t num_splits, void* out, float* lse, float* o_part,
                               float* lse_part, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                               void* stream) {
-  if (num_q < 0 || k <= 0 || page_size <= 0 || num_pages <= 0 || num_req <= 0 || bt_stride <= 0)
-    return DSA_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > 64 || !isfinite(softmax_scale)) return DSA_ERR_INVALID_ARG;
-  if (!supported_shape(num_heads, d_latent, d_rope)) return DSA_ERR_UNSUPPORTED_SHAPE;
-  if (num_pages > (int64_t)INT32_MAX / page_size) return DSA_ERR_UNSUPPORTED_SHAPE;
-  if (num_q == 0) return DSA_OK;
-  const size_t ws_need = dsa_sparse_mla_workspace_size(num_q, num_heads, d_latent, d_rope, k);
-  if (workspace_bytes < ws_need) return DSA_ERR_WORKSPACE_TOO_SMALL;
-  if (ws_need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 7u))) return DSA_ERR_INVALID_ARG;
-  if (!q || !kv || !kv_scale || !block_table || !q_req || !idx) return DSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
-  if (num_splits == 1) {
-    if (!out) return DSA_ERR_INVALID_ARG;
-  } else {
-    if (!o_part || !lse_part || !aligned16(o_part)) return DSA_ERR_INVALID_ARG;
-  }
   dsa::MlaArgs a;
-  a.q = q;
-  a.kv = kv;
-  a.kv_scale = kv_scale;
-  a.num_pages = num_pages;
-  a.block_table = block_table;
-  a.num_req = num_req;
-  a.bt_stride = bt_stride;
-  a.q_req = q_req;
-  a.idx = idx;
-  a.num_q = num_q;
-  a.heads = num_heads;
-  a.d_latent = d_latent;
-  a.d_rope = d_rope;
-  a.page_size = page_size;
-  a.k = k;
-  a.softmax_scale = softmax_scale;
-  a.num_splits = num_splits;
-  a.out = out;
-  a.lse = lse;
-  a.o_part = o_part;
-  a.lse_part = lse_part;
-  a.dev_status = dev_status;
+  const size_t ws_need = dsa_sparse_mla_workspace_size(num_q, num_heads, d_latent, d_rope, k);
+  const dsa_status st = check_mla_args(q, kv, kv_scale, num_pages, block_table, num_req, bt_stride, q_req, idx,
+                                       num_q, num_heads, d_latent, d_rope, page_size, k, softmax_scale, num_splits,
+                                       out, lse, o_part, lse_part, ws_need, workspace, workspace_bytes, dev_status,
+                                       &a);
+  if (st != DSA_OK || num_q == 0) return st;
   if (use_tensor_cores(num_heads, d_latent, d_rope))
     return from_cuda(dsa::launch_mla_tc(a, workspace, static_cast<cudaStream_t>(stream)));
+  return from_cuda(dsa::launch_mla_simt(a, static_cast<cudaStream_t>(stream)));
+}
+
+// Test hook, not part of include/dsa.h: the fp32 CUDA-core kernel on any
+// supported shape, so that tests can cross-check it against the tensor-core
+// kernel on the 64-head shape.  Same arguments as dsa_sparse_mla_fwd minus
+// the workspace (the CUDA-core kernel needs none).
+DSA_API dsa_status dsa_test_sparse_mla_fwd_cuda_cores(const void* q, const uint8_t* kv, const float* kv_scale,
+                                                      int64_t num_pages, const int32_t* block_table, int32_t num_req,
+                                                      int32_t bt_stride, const int32_t* q_req, const int32_t* idx,
+                                                      int32_t num_q, int32_t num_heads, int32_t d_latent,
+                                                      int32_t d_rope, int32_t page_size, int32_t k,
+                                                      float softmax_scale, int32_t num_splits, void* out, float* lse,
+                                                      float* o_part, float* lse_part, int32_t* dev_status,
+                                                      void* stream) {
+  dsa::MlaArgs a;
+  const dsa_status st = check_mla_args(q, kv, kv_scale, num_pages, block_table, num_req, bt_stride, q_req, idx,
+                                       num_q, num_heads, d_latent, d_rope, page_size, k, softmax_scale, num_splits,
+                                       out, lse, o_part, lse_part, 0, nullptr, 0, dev_status, &a);
+  if (st != DSA_OK || num_q == 0) return st;
   return from_cuda(dsa::launch_mla_simt(a, static_cast<cudaStream_t>(stream)));
 }
 

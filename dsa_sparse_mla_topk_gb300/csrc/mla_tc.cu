@@ -13,7 +13,7 @@
 //    Seven TMA warps gather the rows straight from the paged cache into
 //    shared memory with tile::gather4 (four arbitrary rows per copy; 128-byte
 //    swizzle for the 512 latent columns, 64-byte swizzle for the 64 rope
-//    columns; rows past the selection read as zeros); three tiles are in
+//    columns; rows past the selection read as zeros); four tiles are in
 //    flight and no thread touches KV bytes.
 //  * One MMA warp issues kind::f8f6f4 MMAs:
 //        S^T  = K [Q_hi | Q_lo]^T          M = 64 rows, N = 128, K = 576
@@ -34,8 +34,9 @@
 //    lazy rescaling: a head's reference max is raised (and O, l rescaled)
 //    only when a logit exceeds it by more than 2^4, so p <= 16 always.
 //  * TMEM holds two S^T buffers (2 x 128 columns) and O^T (4 x 64 columns);
-//    shared memory holds two P buffers.  QK^T of tile t+1 and the softmax of
-//    tile t run while P V of tile t-1 finishes.  All hand-offs are
+//    shared memory holds one P buffer.  QK^T of tile t+1 and the softmax of
+//    tile t run while P V of tile t-1 finishes; the softmax writes P(t) once
+//    P V of tile t-1 has read P(t-1).  All hand-offs are
 //    mbarriers; every wait is bounded in time and reports DSA_DEV_TIMEOUT
 //    instead of hanging.
 //  * A small resolve kernel first turns every selected position into its
@@ -60,7 +61,7 @@ using namespace sm100;
 
 constexpr int H = 64, DL = 512, DR = 64, DQK = DL + DR;
 constexpr int T = 64;                            // KV rows per tile
-constexpr int NST = 3;                           // KV tiles in flight
+constexpr int NST = 4;                           // KV tiles in flight
 constexpr int NLAT = DL / 128;                   // 128-column latent slices per row: 4
 constexpr int LAT_BYTES = T * 128;               // one latent slice of a tile (128-byte swizzle)
 constexpr int ROPE_OFF = NLAT * LAT_BYTES;       // the rope slice (64-byte swizzle)
@@ -89,8 +90,8 @@ constexpr uint32_t TM_S = 0, TM_O = 256, TM_COLS = 512;
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int OFF_KV = 0;
 constexpr int OFF_Q = OFF_KV + NST * STAGE_BYTES;
-constexpr int OFF_P = OFF_Q + Q_BYTES;               // [buffer][hi, lo]
-constexpr int OFF_RED = OFF_P + 2 * 2 * P_BYTES;     // [4 quadrants][64 heads] floats
+constexpr int OFF_P = OFF_Q + Q_BYTES;               // [hi, lo]: one buffer
+constexpr int OFF_RED = OFF_P + 2 * P_BYTES;         // [4 quadrants][64 heads] floats
 constexpr int OFF_MUSE = OFF_RED + 4 * H * 4;        // reference max per head (log2 domain)
 constexpr int OFF_ALPHA = OFF_MUSE + H * 4;
 constexpr int OFF_FLAG = OFF_ALPHA + H * 4;          // votes [2][8], rescale flags [2], Q exponent
@@ -98,17 +99,19 @@ constexpr int OFF_BAR = OFF_FLAG + 128;
 constexpr int B_KVF = 0;                  // [NST] tile in stage s has landed (TMA transaction bytes)
 constexpr int B_KVE = B_KVF + NST;        // [NST] stage s is free (its P V MMAs are done)
 constexpr int B_SF = B_KVE + NST;         // [2] S^T buffer b is complete
-constexpr int B_PF = B_SF + 2;            // [2] P buffer b is written (and O rescaled)
-constexpr int B_PVD = B_PF + 2;           // [2] P V of the tile in P buffer b is done
-constexpr int B_OF = B_PVD + 2;           // every P V is done
+constexpr int B_PF = B_SF + 2;            // P of the next tile is written (and O rescaled)
+constexpr int B_PVD = B_PF + 1;           // P V of a tile is done (one phase per tile): P is free
+constexpr int B_OF = B_PVD + 1;           // every P V is done
 constexpr int B_SYNCA = B_OF + 1;         // softmax-group sync points
 constexpr int B_SYNCB = B_SYNCA + 1;
 constexpr int B_SYNCC = B_SYNCB + 1;
 constexpr int B_FIN = B_SYNCC + 1;        // every MMA is done (teardown)
-constexpr int B_QREADY = B_FIN + 1;       // Q hi/lo is in shared memory (and stages 1, 2 are free)
-constexpr int B_QLOAD = B_QREADY + 1;     // raw bf16 Q has landed in stages 1, 2
+constexpr int B_QREADY = B_FIN + 1;       // Q hi/lo is in shared memory (and the Q staging stages are free)
+constexpr int B_QLOAD = B_QREADY + 1;     // raw bf16 Q has landed in the staging stages
 constexpr int NBAR = B_QLOAD + 1;
-static_assert(2 * STAGE_BYTES == H * DQK * 2, "bf16 Q is staged in KV stages 1 and 2");
+constexpr int QSTAGE = NST - 2;           // raw bf16 Q is staged in KV stages NST - 2 and NST - 1
+static_assert(2 * STAGE_BYTES == H * DQK * 2, "bf16 Q fills two KV stages");
+static_assert(NST * STAGE_BYTES >= H * DL * 4, "the epilogue stages O (fp32 partials) in the KV stages");
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_TMEM + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
@@ -282,11 +285,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_KVF + s), NTMA);
       mbar_init(bar(B_KVE + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_SF + b), 1);
-      mbar_init(bar(B_PF + b), SOFTMAX_WARPS);
-      mbar_init(bar(B_PVD + b), 1);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(bar(B_SF + b), 1);
+    mbar_init(bar(B_PF), SOFTMAX_WARPS);
+    mbar_init(bar(B_PVD), 1);
     mbar_init(bar(B_OF), 1);
     mbar_init(bar(B_SYNCA), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCB), SOFTMAX_WARPS);
@@ -312,15 +313,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t kv_base = smem_u32(smem + OFF_KV), q_base = smem_u32(q_s), p_base = smem_u32(p_s);
   bool ok = true;
 
-  // Q of this token: bf16 [64 heads][576] (bulk-copied into KV stages 1
-  // and 2) -> x 2^qexp -> E4M3 hi (B rows 0..63) and lo (B rows 64..127),
-  // K-major, in the MMA's swizzled layouts.  Done by the TMA warps (once the
-  // copies of tile 0 are out) and the softmax warps together: qt numbers
-  // their NQ threads; named barrier 1 syncs them.
+  // Q of this token: bf16 [64 heads][576] (bulk-copied into the two staging
+  // KV stages) -> x 2^qexp -> E4M3 hi (B rows 0..63) and lo (B rows
+  // 64..127), K-major, in the MMA's swizzled layouts.  Done by the TMA warps
+  // (once the copies of tile 0 are out) and the softmax warps together: qt
+  // numbers their NQ threads; named barrier 1 syncs them.
   constexpr int NQ = (NTMA + SOFTMAX_WARPS) * 32;
   auto convert_q = [&](int qt) {
     constexpr int CH = DQK / 8;  // 16-byte chunks (8 bf16) per head
-    const uint4* qraw = reinterpret_cast<const uint4*>(smem + OFF_KV + STAGE_BYTES);
+    const uint4* qraw = reinterpret_cast<const uint4*>(smem + OFF_KV + QSTAGE * STAGE_BYTES);
     auto bf_lo = [](uint32_t w) { return __uint_as_float(w << 16); };
     auto bf_hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
     if (!wait_warp(B_QLOAD, 0)) ok = false;
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       *reinterpret_cast<uint2*>(q_s + off_lo) = lv;
     }
     // the raw Q reads and the hi/lo writes are ordered before the TMA
-    // warps' next copies into stages 1, 2 and before the MMAs
+    // warps' next copies into the staging stages and before the MMAs
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(B_QREADY));
@@ -384,9 +385,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int my_groups = (GROUPS - tw + NTMA - 1) / NTMA;
     const int g = tw + NTMA * lane;
     int issued = 0;
-    if (tw == 0 && lane == 0) {  // raw Q into stages 1 and 2, converted by the softmax warps
+    if (tw == 0 && lane == 0) {  // raw Q into the staging stages, converted by all but the MMA warp
       mbar_arrive_expect_tx(bar(B_QLOAD), 2 * STAGE_BYTES);
-      tma_bulk_load(kv_base + STAGE_BYTES, static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK,
+      tma_bulk_load(kv_base + QSTAGE * STAGE_BYTES, static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK,
                     2 * STAGE_BYTES, bar(B_QLOAD));
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the resolve kernel's entries are complete
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = false;
         break;
       }
-      if (lt == 1 && !wait_warp(B_QREADY, 0)) {  // stages 1 and 2 hold raw Q until then
+      if (lt == QSTAGE && !wait_warp(B_QREADY, 0)) {  // the staging stages hold raw Q until then
         ok = false;
         break;
       }
@@ -445,9 +446,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     // the 4 independent d-chunks innermost: consecutive MMAs never share an accumulator
     auto issue_pv = [&](int lt) {
-      const int s = lt % NST, pb = lt & 1;
+      const int s = lt % NST;
       const uint64_t a0 = smem_desc(kv_base + s * STAGE_BYTES, LAT_BYTES, 1024, SWIZZLE_128B);
-      const uint64_t b0 = smem_desc(p_base + pb * 2 * P_BYTES, P_BYTES, 512, SWIZZLE_64B);
+      const uint64_t b0 = smem_desc(p_base, P_BYTES, 512, SWIZZLE_64B);
 #pragma unroll
       for (int w = 0; w < 2; ++w) {
 #pragma unroll
@@ -459,7 +460,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       mma_commit_warp(bar(B_KVE + s));
-      mma_commit_warp(bar(B_PVD + pb));
+      mma_commit_warp(bar(B_PVD));
     };
     ok = wait_warp(B_QREADY, 0) && wait_warp(B_KVF, 0);
     if (ok) {
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after_sync();
         issue_qk(lt + 1);
       }
-      if (!wait_warp(B_PF + (lt & 1), (lt >> 1) & 1)) {
+      if (!wait_warp(B_PF, lt & 1)) {
         ok = false;
         break;
       }
@@ -612,7 +613,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (resc_s[h2]) {
           // O must hold every P V issued so far: the previous tile's
-          if (!wait_warp(B_PVD + (sb ^ 1), ((lt - 1) >> 1) & 1)) {
+          if (!wait_warp(B_PVD, (lt - 1) & 1)) {
             ok = false;
             break;
           }
@@ -637,13 +638,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         load_z(z);  // S is still in TMEM: reload rather than keep z live across the rescale
       }
-      // the P buffer is free once P V of the tile two back is done
-      if (lt >= 2 && !wait_warp(B_PVD + sb, ((lt - 2) >> 1) & 1)) {
-        ok = false;
-        break;
-      }
       // probabilities, folded with the row's dequantisation scale and the
-      // query's power of two, as E4M3 hi + lo
+      // query's power of two, as E4M3 hi + lo (computed before waiting for
+      // the P buffer, so that only the stores wait)
       uint32_t phi[8], plo[8];
       const float sp = sc * p_scale;
       const float4* mu4 = reinterpret_cast<const float4*>(muse_s + 16 * hg);
@@ -661,8 +658,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           split_e4m3x2(f32x2_to_f16x2(p0 * sp, p1 * sp), phi[h / 2], plo[h / 2]);
         }
       }
+      // the P buffer is free once P V of the previous tile is done
+      if (lt >= 1 && !wait_warp(B_PVD, (lt - 1) & 1)) {
+        ok = false;
+        break;
+      }
       {
-        unsigned char* pr = p_s + sb * 2 * P_BYTES + j * H + ((hg ^ ((j >> 1) & 3)) << 4);
+        unsigned char* pr = p_s + j * H + ((hg ^ ((j >> 1) & 3)) << 4);
         *reinterpret_cast<uint4*>(pr) = make_uint4(phi[0] | (phi[1] << 16), phi[2] | (phi[3] << 16),
                                                    phi[4] | (phi[5] << 16), phi[6] | (phi[7] << 16));
         *reinterpret_cast<uint4*>(pr + P_BYTES) = make_uint4(plo[0] | (plo[1] << 16), plo[2] | (plo[3] << 16),
@@ -671,7 +673,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PF + sb));
+      if (lane == 0) mbar_arrive(bar(B_PF));
       info = info_next;
     }
     // ---------------- epilogue: normalise and write ----------------
@@ -697,7 +699,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = group_sync(B_SYNCC, ph_c);
     }
     if (ok) {
+      // O^T (TMEM) -> normalised rows in the (now idle) KV stages, laid out
+      // as the output [head][d], then one bulk copy to global memory: the
+      // token's 64 x 512 result is contiguous (bf16, or fp32 for a split).
       const float* inv = alpha_s + 32 * h2;
+      unsigned char* stg = smem + OFF_KV;
 #pragma unroll 1
       for (int c = 0; c < NLAT; ++c) {
         const int d = 128 * c + 32 * q4 + lane;
@@ -710,13 +716,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int h = 0; h < 16; ++h) {
             const int hh = 32 * h2 + 16 * g + h;
             const float val = o[h] * inv[16 * g + h];
-            const int64_t off = ((int64_t)i * H + hh) * DL + d;
             if (S == 1)
-              static_cast<__nv_bfloat16*>(a.out)[off] = __float2bfloat16_rn(val);
+              reinterpret_cast<__nv_bfloat16*>(stg)[hh * DL + d] = __float2bfloat16_rn(val);
             else
-              a.o_part[(int64_t)split * a.num_q * H * DL + off] = val;
+              reinterpret_cast<float*>(stg)[hh * DL + d] = val;
           }
         }
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(2, SOFTMAX_WARPS * 32);
+      // 16 KB pieces, one per lane of softmax warp 0 (4 for bf16, 8 for fp32)
+      const uint32_t piece = 16384, bytes = (uint32_t)(H * DL * (S == 1 ? 2 : 4));
+      if (sw == 0 && lane * piece < bytes) {
+        unsigned char* dst = S == 1
+                                 ? reinterpret_cast<unsigned char*>(static_cast<__nv_bfloat16*>(a.out) + (int64_t)i * H * DL)
+                                 : reinterpret_cast<unsigned char*>(a.o_part + ((int64_t)split * a.num_q + i) * H * DL);
+        tma_bulk_store(dst + lane * piece, smem_u32(stg) + lane * piece, piece);
+        tma_bulk_store_wait_read();  // the shared memory stays valid until the copy has read it
       }
     } else if (lane == 0) {
       report(a.dev_status, DSA_DEV_TIMEOUT);

@@ -26,6 +26,10 @@
 //  * The device address of the array is looked up once per device, with that
 //    device current, on the first call made while it is the current device.
 //    Make that first call before starting any stream capture on the device.
+//  * That address is kept for the life of the process.  A device reset
+//    (cudaDeviceReset, or a reset of the primary context) reloads the library
+//    image and moves the array, so this entry point must not be used after
+//    one.
 #include <cuda_runtime.h>
 
 #include <mutex>

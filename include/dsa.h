@@ -136,7 +136,7 @@ DSA_API size_t dsa_topk_workspace_size(int32_t num_q, int64_t ld_scores, int32_t
  *   q_req        int32 [num_q] request of each query token, in [0, num_req).
  *   idx          int32 [num_q, k] selected positions (-1 = none), any order.
  *   num_splits   1..64.  With 1 the call writes out (bf16 [num_q, heads,
- *                d_latent]) and lse (fp32 [num_q, heads]).  With S > 1 the k
+ *                d_latent], 16-byte aligned) and lse (fp32 [num_q, heads]).  With S > 1 the k
  *                entries of each row are cut into S contiguous chunks of whole
  *                KV tiles and the call writes o_part (fp32 [S, num_q, heads,
  *                d_latent]) and lse_part (fp32 [S, num_q, heads]) instead, to
@@ -179,8 +179,10 @@ DSA_API size_t dsa_sparse_mla_workspace_size(int32_t num_q, int32_t num_heads, i
  * the array: calls whose GPU work overlaps (unordered streams, concurrent
  * host threads) race and must be serialised by the caller.  The first call on
  * a device, made with that device current, looks up the array's device
- * address; make it before any stream capture on that device.  The call
- * allocates nothing.
+ * address; make it before any stream capture on that device.  That address
+ * is kept for the life of the process: do not call this entry point again
+ * after a device reset (cudaDeviceReset, or a reset of the primary context),
+ * which moves the array.  The call allocates nothing.
  */
 DSA_API dsa_status dsa_sparse_mla_fwd_noalloc(const void* q, const uint8_t* kv, const float* kv_scale,
                                               int64_t num_pages, const int32_t* block_table, int32_t num_req,

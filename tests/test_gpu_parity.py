@@ -128,19 +128,22 @@ def test_topk_whole_index_array_bit_exact(w):
         assert np.array_equal(host(idx2), ref)
 
 
-def test_topk_prefill_rows_bit_exact_sampled():
+def test_topk_prefill_whole_index_array_bit_exact():
+    """Every one of the 32,768 prefill rows (not a sample): the row kernel's
+    sample / screen / fallback decisions depend on each row's data, so the
+    whole index array is compared with the oracle, in chunks of rows that the
+    host holds comfortably."""
     w = wl.PREFILL_32K
     inp = inputs(w)
     idx = dsa.topk_select(inp.scores, inp.q_pos, w.k)
     torch.cuda.synchronize()
-    rows = sample_rows(w.num_q, 256, seed=5)
-    rt = torch.as_tensor(rows, device="cuda")
-    ref = oracle.topk(host(inp.scores.index_select(0, rt)), host(inp.q_pos)[rows], w.k)
-    assert np.array_equal(host(idx)[rows], ref)
-    # every row: ascending, unique, in range
-    i = idx.long()
-    assert bool((i[:, 1:] > i[:, :-1]).all())
-    assert bool((i >= 0).all()) and bool((i <= inp.q_pos.long()[:, None]).all())
+    got = host(idx)
+    q_pos = host(inp.q_pos)
+    chunk = 2048
+    for r0 in range(0, w.num_q, chunk):
+        r1 = min(w.num_q, r0 + chunk)
+        ref = oracle.topk(host(inp.scores[r0:r1]), q_pos[r0:r1], w.k)
+        assert np.array_equal(got[r0:r1], ref), f"rows {r0}..{r1 - 1} differ from the oracle"
 
 
 @pytest.mark.parametrize("w", [wl.TINY, SMALL_H64], ids=lambda w: w.name)
@@ -260,39 +263,72 @@ def test_permuted_indices_give_same_output():
     assert (o1.float() - o2.float()).abs().max().item() <= 4e-3
 
 
-def test_tensor_core_kernel_matches_cuda_core_kernel(monkeypatch):
+def test_tensor_core_kernel_matches_cuda_core_kernel():
     """The tcgen05 kernel and the fp32 CUDA-core kernel agree on the same
-    selection (both are also checked against the oracle above)."""
+    selection (both are also checked against the oracle above).  The CUDA-core
+    kernel runs on the 64-head shape only through the library's test hook;
+    the product entry point always takes the tensor cores for that shape."""
+    import ctypes
     w = SMALL_H64
     inp = inputs(w)
     idx = dsa.topk_select(inp.scores, inp.q_pos, w.k)
     kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
     o_tc, l_tc = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, **kw)
-    torch.cuda.synchronize()
-    monkeypatch.setenv("DSA_FORCE_SIMT", "1")
-    o_s, l_s = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, **kw)
+    o_s = torch.empty_like(o_tc)
+    l_s = torch.empty_like(l_tc)
+    lib = dsa.load_library()
+    fn = lib.dsa_test_sparse_mla_fwd_cuda_cores
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    fn.argtypes = [vp, vp, vp, i64, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32, ctypes.c_float, i32, vp, vp,
+                   vp, vp, vp, vp]
+    fn.restype = i32
+    p = lambda t: vp(t.data_ptr())
+    st = fn(p(inp.q), p(inp.kv), p(inp.kv_scale), inp.kv.shape[0] // w.page_size, p(inp.block_table),
+            inp.block_table.shape[0], inp.block_table.shape[1], p(inp.q_req), p(idx), w.num_q, w.heads, w.d_latent,
+            w.d_rope, w.page_size, w.k, w.scale, 1, p(o_s), p(l_s), None, None, None,
+            vp(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
     torch.cuda.synchronize()
     assert (o_tc.float() - o_s.float()).abs().max().item() <= 4e-3
     assert (l_tc - l_s).abs().max().item() <= 1e-3
 
 
-def test_large_logit_range_triggers_rescale():
-    """Queries scaled up so that later tiles raise the running max by far more
-    than the lazy-rescale threshold: the result must still match the oracle."""
-    w = wl.Workload("rescale_h64", 2, 2, 64, 512, 64, 1500, 0, 64, 1024, seed=31)
+def test_peaked_softmax_within_task_tolerance():
+    """A peaked softmax checked at the benchmark's tolerance (max-abs 1e-2,
+    relative L2 5e-3).  The logits are those of queries scaled by 6 (~ N(0,
+    36)), so later tiles raise the running maximum past the lazy-rescale
+    threshold and the accumulators are rescaled.  The KV scales are divided by
+    4 and the queries multiplied by 24 instead of 6, which leaves the logits
+    unchanged but keeps the values, and so the outputs, below 2 in magnitude:
+    from 4 upwards bf16 itself spaces its values 2^-5 apart, so no bf16
+    output could be held to an absolute 1e-2 there."""
+    w = wl.Workload("rescale6_h64", 2, 2, 64, 512, 64, 1500, 0, 64, 1024, seed=31)
     inp = wl.make_inputs(w, device="cuda")
-    # large queries: logits ~ N(0, 400), so later tiles beat the first tile's
-    # maximum by more than 2^8 and the accumulators must be rescaled
+    inp.kv_scale.mul_(0.25)
+    inp.q.mul_(24.0)
+    out, lse, idx = run(inp)
+    rows = np.arange(w.num_q)
+    ref_idx, ref_out, ref_lse = oracle_rows(inp, rows)
+    assert np.array_equal(host(idx), ref_idx)
+    assert float(np.abs(ref_out).max()) < 2.0
+    assert_close(host(out.float()), host(lse), ref_out, ref_lse, "peaked")
+
+
+def test_very_peaked_softmax_stress_derived_bound():
+    """Stress case beyond the workloads: queries scaled by 20 (logits ~
+    N(0, 400)), so later tiles beat the first tile's maximum by more than 2^8
+    and the accumulators are rescaled many times.  Outputs are then as large
+    as single value rows, and the bound checked is the one the arithmetic
+    gives rather than the task's absolute 1e-2: the weights carry 8
+    significant bits (relative 2^-9 each) and O is rounded to bf16 (relative
+    2^-9), so |error| <= 2^-9 (max|O| + max|V|)."""
+    w = wl.Workload("rescale20_h64", 2, 2, 64, 512, 64, 1500, 0, 64, 1024, seed=31)
+    inp = wl.make_inputs(w, device="cuda")
     inp.q.mul_(20.0)
     out, lse, idx = run(inp)
     rows = np.arange(w.num_q)
     ref_idx, ref_out, ref_lse = oracle_rows(inp, rows)
     assert np.array_equal(host(idx), ref_idx)
-    # Such peaked softmaxes give outputs as large as single value rows, so
-    # the roundings of P (8 significant bits on the tensor-core path, E4M3
-    # hi + lo: relative 2^-9 per weight) and of O (bf16, relative 2^-9) bound
-    # the error by 2^-9 (max|O| + max|V|), above the absolute 1e-2 of the
-    # N(0,1) workloads; that derived bound is the check here.
     max_v = float((inp.kv_scale.max() * 448.0).item())
     tol = 2.0 ** -9 * (float(np.abs(ref_out).max()) + max_v)
     got = host(out.float()).astype(np.float64)
