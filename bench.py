@@ -34,15 +34,10 @@ L2_FLUSH_BYTES = 512 << 20
 NOMINAL_TFLOPS, NOMINAL_GBS = 2250.0, 8000.0
 FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 
-# DRAM bytes (read + write) per launch of the attention kernel, from one ncu
-# capture, keyed by the SHA-1 of the kernel source it was taken on.  A stale
-# entry (the kernel changed since) is reported as null.
-TRAFFIC_BY_SOURCE: dict[str, dict] = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, second launch,
-    # decode_64k_prefix99.9: 49,051,904 B read + 513,536 B written
-    # (profiles/mla_tc_kernel_decode_64k_prefix99.9.md)
-    "fc7175a5ace561c212cec24b55beffdae6d83db8": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49565440},
-}
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture, keyed by the SHA-1 of the kernel sources it was taken on (reported
+# as null once those sources change).
+TRAFFIC_BY_SOURCE: dict[str, dict] = {}
 
 
 def parse_args():
@@ -51,7 +46,13 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_64k_prefix99.9")
+    ap.add_argument("--workload", default="decode_64k_prefix99.9", help="the headline workload")
+    ap.add_argument("--also", default="verify_64k_8tok",
+                    help="further workloads measured in the same run (comma separated; '' for none)")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the timed block of --steps passes until about this much timed load")
+    ap.add_argument("--max-blocks", type=int, default=400)
+    ap.add_argument("--no-fused", action="store_true", help="run top-k and attention as separate calls")
     ap.add_argument("--splits", type=int, default=0, help="KV splits (0 = library's rule)")
     ap.add_argument("--cpu-sample", type=int, default=64, help="query tokens the oracle baseline times")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -268,6 +269,157 @@ def bench_reference(args):
     return 0
 
 
+def prepare(w, dev, dsa, wl, args, torch):
+    """Inputs, buffers and launch choices of one workload."""
+    inp = wl.make_inputs(w, device=dev)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    S = args.splits or dsa.pick_num_splits(w.num_q, w.heads, w.d_latent, w.d_rope, w.k, num_sms)
+    fused = (not args.no_fused) and dsa.use_fused_path(w.num_q, w.heads, w.d_latent, w.d_rope, inp.scores.shape[1],
+                                                        w.k, S, dev)
+    bufs = {"idx": torch.empty((w.num_q, w.k), dtype=torch.int32, device=dev),
+            "out": torch.empty((w.num_q, w.heads, w.d_latent), dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty((w.num_q, w.heads), dtype=torch.float32, device=dev)}
+    if S > 1:
+        bufs["o_part"] = torch.empty((S, w.num_q, w.heads, w.d_latent), dtype=torch.float32, device=dev)
+        bufs["lse_part"] = torch.empty((S, w.num_q, w.heads), dtype=torch.float32, device=dev)
+    ws_bytes = dsa.sparse_mla_workspace_size(w.num_q, w.heads, w.d_latent, w.d_rope, w.k)
+    if ws_bytes:
+        bufs["workspace"] = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    topk_ws = dsa.topk_workspace_size(w.num_q, inp.scores.shape[1], w.k)
+    if topk_ws:
+        bufs["topk_workspace"] = torch.empty(topk_ws, dtype=torch.uint8, device=dev)
+    flops, bytes_fwd, bytes_topk = algorithmic(w, inp.q_pos.cpu().numpy())
+    kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+    # kernels of this library launched by one pass
+    if fused:
+        launches = 1
+    else:
+        launches = (2 if topk_ws else 1) + (2 if ws_bytes else 1) + (1 if S > 1 else 0)
+    return {"w": w, "inp": inp, "S": S, "fused": fused, "bufs": bufs, "kw": kw, "flops": flops,
+            "bytes_fwd": bytes_fwd, "bytes_topk": bytes_topk, "launches": launches, "ws_bytes": ws_bytes}
+
+
+def one_pass(dsa, c, stream, status):
+    """One pass of the whole path through the public call (top-k -> Partial
+    -> Combine when split; top-k and Partial in one kernel on the fused path)."""
+    w, inp = c["w"], c["inp"]
+    dsa.sparse_mla_topk(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, inp.q_pos, inp.scores, w.k,
+                        num_splits=c["S"], buffers=c["bufs"], dev_status=status, stream=stream, fused=c["fused"],
+                        **c["kw"])
+
+
+def separate_calls(dsa, c, stream, status, evs):
+    """The same pass as separate calls with events between them: top-k,
+    the attention call (resolve + Partial), the Combine."""
+    w, inp, S, bufs, kw = c["w"], c["inp"], c["S"], c["bufs"], c["kw"]
+    evs[0].record(stream)
+    idx = dsa.topk_select(inp.scores, inp.q_pos, w.k, idx=bufs["idx"], dev_status=status, stream=stream,
+                          workspace=bufs.get("topk_workspace"))
+    evs[1].record(stream)
+    if S == 1:
+        dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, num_splits=1, out=bufs["out"],
+                           lse=bufs["lse"], workspace=bufs.get("workspace"), dev_status=status, stream=stream, **kw)
+    else:
+        dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, num_splits=S,
+                           o_part=bufs["o_part"], lse_part=bufs["lse_part"], workspace=bufs.get("workspace"),
+                           dev_status=status, stream=stream, **kw)
+    evs[2].record(stream)
+    if S > 1:
+        dsa.combine(bufs["o_part"], bufs["lse_part"], out=bufs["out"], lse=bufs["lse"], stream=stream)
+    evs[3].record(stream)
+
+
+def measure(dsa, c, args, torch, dev, stream, status, flush, world, barrier, peaks):
+    """Time exactly K = args.steps passes per block, L2 flushed before every
+    pass, blocks repeated until about args.min_seconds of timed load; then the
+    separate calls once more for the per-kernel breakdown.  Returns the
+    workload's report."""
+    w = c["w"]
+    K = args.steps
+    for _ in range(args.warmup):
+        flush.zero_()
+        one_pass(dsa, c, stream, status)
+    torch.cuda.synchronize(dev)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    def block():
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        barrier()
+        for s in range(K):
+            flush.zero_()
+            evs[s][0].record(stream)
+            one_pass(dsa, c, stream, status)
+            evs[s][1].record(stream)
+        barrier()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    t0 = time.perf_counter()
+    first = block()
+    wall = max_over_ranks(time.perf_counter() - t0, world, dev)
+    nblocks = max(1, min(args.max_blocks, int(max_over_ranks(args.min_seconds / max(wall, 1e-6), world, dev)) + 1))
+    per_block, step_ms = [], []
+    for _ in range(nblocks):
+        ms = block()
+        step_ms += ms
+        per_block.append(max_over_ranks(sum(ms), world, dev))
+    del first
+    block_ms = statistics.median(per_block)
+    value = whole_job_rate(world, w.num_q, K, block_ms)
+    ms_per_step = block_ms / K
+
+    # per-kernel breakdown from the separate calls (the fused path runs them as one kernel)
+    comp = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(max(10, K))]
+    for e in comp:
+        flush.zero_()
+        separate_calls(dsa, c, stream, status, e)
+    torch.cuda.synchronize(dev)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    t_topk = statistics.median(e[0].elapsed_time(e[1]) for e in comp)
+    t_fwd = statistics.median(e[1].elapsed_time(e[2]) for e in comp)
+    t_comb = statistics.median(e[2].elapsed_time(e[3]) for e in comp)
+    t_sep = statistics.median(e[0].elapsed_time(e[3]) for e in comp)
+
+    flops, bytes_fwd, bytes_topk = c["flops"], c["bytes_fwd"], c["bytes_topk"]
+    bytes_path = bytes_fwd + bytes_topk
+    ai_path = flops / bytes_path
+    ns_roof = min(NOMINAL_TFLOPS * 1e12, NOMINAL_GBS * 1e9 * ai_path)
+    meas_roof = min(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9 * ai_path)
+    achieved_flops = flops / (ms_per_step / 1e3)
+    src_files = ["mla_tc.cu", "topk_row.cuh"] if c["fused"] else ["mla_tc.cu"]
+    sha = hashlib.sha1(b"".join(open(os.path.join(ROOT, "dsa_sparse_mla_topk_gb300", "csrc", f), "rb").read()
+                                for f in src_files)).hexdigest()
+    tr = TRAFFIC_BY_SOURCE.get(sha)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("workload") == w.name else None
+    if c["fused"]:
+        # the one kernel is the whole pass: its algorithmic bytes are the pass's
+        kern, kbytes, kms = "sparse_mla_topk_fwd (top-k + attention, one kernel)", bytes_path, ms_per_step
+    else:
+        kern, kbytes, kms = "sparse_mla_fwd (resolve + attention)", bytes_fwd, t_fwd
+    achieved_gbs = kbytes / (kms / 1e3) / 1e9
+    att_ms = t_fwd + (t_comb if c["S"] > 1 else 0.0)
+    return {
+        "workload": w.name, "value": value, "unit": UNIT, "query_tokens": w.num_q, "steps": K, "blocks": nblocks,
+        "ms_per_step": ms_per_step,
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms),
+                    "count": len(step_ms)},
+        "path": "fused" if c["fused"] else "separate calls", "kv_splits": c["S"],
+        "gpu_launches_per_step": c["launches"],
+        "roofline": {"kernel": kern, "bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": peaks["source"], "algorithmic_bytes_per_launch": kbytes, "avg_launch_ms": kms,
+                     "achieved_tflops": flops / (kms / 1e3) / 1e12},
+        "path_roofline": {"ai_flops_per_byte": ai_path, "achieved_tflops": achieved_flops / 1e12,
+                          "frac_nominal": achieved_flops / ns_roof, "frac_measured": achieved_flops / meas_roof,
+                          "nominal_roofline_tflops": ns_roof / 1e12},
+        "kernel_ms_separate_calls": {"topk": t_topk, "sparse_mla_fwd": t_fwd, "combine": t_comb, "pass": t_sep},
+        "attention_only": {"value": w.num_q / (att_ms / 1e3), "unit": UNIT,
+                           "note": "the attention call (resolve + Partial) plus the Combine when split, timed as "
+                                   "separate calls with L2 flushed",
+                           "achieved_gbs": bytes_fwd / (att_ms / 1e3) / 1e9,
+                           "frac_hbm": bytes_fwd / (att_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+    }
+
+
 def bench_ours(args):
     import numpy as np
     import torch
@@ -286,86 +438,38 @@ def bench_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     lib_build.build()
     dsa.load_library()
+    peaks = read_peaks()
 
-    w = wl.WORKLOADS[args.workload]
-    inp = wl.make_inputs(w, device=dev)
-    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    S = args.splits or dsa.pick_num_splits(w.num_q, w.heads, w.d_latent, w.d_rope, w.k, num_sms)
-    q_pos_host = inp.q_pos.cpu().numpy()
-    flops, bytes_fwd, bytes_topk = algorithmic(w, q_pos_host)
-    bytes_path = bytes_fwd + bytes_topk
-
+    names = [args.workload] + [n for n in args.also.split(",") if n and n != args.workload]
     stream = torch.cuda.current_stream(dev)
-    bufs = {"idx": torch.empty((w.num_q, w.k), dtype=torch.int32, device=dev),
-            "out": torch.empty((w.num_q, w.heads, w.d_latent), dtype=torch.bfloat16, device=dev),
-            "lse": torch.empty((w.num_q, w.heads), dtype=torch.float32, device=dev)}
-    if S > 1:
-        bufs["o_part"] = torch.empty((S, w.num_q, w.heads, w.d_latent), dtype=torch.float32, device=dev)
-        bufs["lse_part"] = torch.empty((S, w.num_q, w.heads), dtype=torch.float32, device=dev)
-    ws_bytes = dsa.sparse_mla_workspace_size(w.num_q, w.heads, w.d_latent, w.d_rope, w.k)
-    if ws_bytes:
-        bufs["workspace"] = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    topk_ws = dsa.topk_workspace_size(w.num_q, inp.scores.shape[1], w.k)
-    if topk_ws:
-        bufs["topk_workspace"] = torch.empty(topk_ws, dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
-
-    def step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        idx = dsa.topk_select(inp.scores, inp.q_pos, w.k, idx=bufs["idx"], dev_status=status, stream=stream,
-                              workspace=bufs.get("topk_workspace"))
-        if evs:
-            evs[1].record(stream)
-        if S == 1:
-            dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, num_splits=1,
-                               out=bufs["out"], lse=bufs["lse"], workspace=bufs.get("workspace"), dev_status=status,
-                               stream=stream, **kw)
-        else:
-            dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, idx, num_splits=S,
-                               o_part=bufs["o_part"], lse_part=bufs["lse_part"], workspace=bufs.get("workspace"),
-                               dev_status=status, stream=stream, **kw)
-        if evs:
-            evs[2].record(stream)
-        if S > 1:
-            dsa.combine(bufs["o_part"], bufs["lse_part"], out=bufs["out"], lse=bufs["lse"], stream=stream)
-        if evs:
-            evs[3].record(stream)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clock_path = args.clocks_csv.format(rank=rank) if args.clocks_csv else None
     sampler = ClockSampler(gpu_uuid(torch, dev), clock_path) if not args.no_clocks else None
+    reports = {}
+    head = None
     if sampler:
         sampler.__enter__()
-    barrier()
     wall0 = time.perf_counter()
-    for s in range(args.steps):
-        flush.zero_()
-        step(evs[s])
-    barrier()
+    for n in names:
+        c = prepare(wl.WORKLOADS[n], dev, dsa, wl, args, torch)
+        reports[n] = measure(dsa, c, args, torch, dev, stream, status, flush, world, barrier, peaks)
+        if head is None:
+            head = c
+        else:
+            del c
+            torch.cuda.empty_cache()
     wall = time.perf_counter() - wall0
     if sampler:
         sampler.__exit__(None, None, None)
-    t_topk = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
-    t_fwd = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
-    t_comb = [evs[s][2].elapsed_time(evs[s][3]) for s in range(args.steps)]
-    t_step = [evs[s][0].elapsed_time(evs[s][3]) for s in range(args.steps)]
-    total_ms = max_over_ranks(sum(t_step), world, dev)
-    ms_per_step = total_ms / args.steps
-    value = whole_job_rate(world, w.num_q, args.steps, total_ms)
+    w, inp, S, bufs, kw = head["w"], head["inp"], head["S"], head["bufs"], head["kw"]
+    rep = reports[w.name]
 
     # ---- end to end through host buffers: copies timed every step ----
     # Every step copies its own inputs from pinned host memory and reads its
@@ -374,21 +478,22 @@ def bench_ours(args):
     # buffered, and L2 is still flushed before every step's compute.
     e2e = None
     if not args.no_e2e:
-        names = ("q", "scores", "q_pos", "q_req", "block_table")
-        pin = {n: getattr(inp, n).cpu().pin_memory() for n in names}
+        names_in = ("q", "scores", "q_pos", "q_req", "block_table")
+        pin = {n: getattr(inp, n).cpu().pin_memory() for n in names_in}
         NB = 2
-        dsts = [{n: torch.empty_like(getattr(inp, n)) for n in names} for _ in range(NB)]
+        dsts = [{n: torch.empty_like(getattr(inp, n)) for n in names_in} for _ in range(NB)]
         outs = [torch.empty_like(bufs["out"]) for _ in range(NB)]
         lses = [torch.empty_like(bufs["lse"]) for _ in range(NB)]
+        idxs = [torch.empty_like(bufs["idx"]) for _ in range(NB)]
         out_h = [torch.empty(bufs["out"].shape, dtype=bufs["out"].dtype).pin_memory() for _ in range(NB)]
         lse_h = [torch.empty(bufs["lse"].shape, dtype=bufs["lse"].dtype).pin_memory() for _ in range(NB)]
         h2d = sum(t.numel() * t.element_size() for t in pin.values())
         d2h = out_h[0].numel() * out_h[0].element_size() + lse_h[0].numel() * lse_h[0].element_size()
         cs = [torch.cuda.Stream(dev) for _ in range(max(1, args.copy_streams))]
 
-        def rows_of(t, c):  # stream c's share of tensor t's rows
-            n = t.shape[0]
-            return slice(n * c // len(cs), n * (c + 1) // len(cs))
+        def rows_of(t, ci):  # stream ci's share of tensor t's rows
+            nrow = t.shape[0]
+            return slice(nrow * ci // len(cs), nrow * (ci + 1) // len(cs))
 
         def ev():
             return torch.cuda.Event(enable_timing=True)
@@ -400,17 +505,17 @@ def bench_ours(args):
 
             def issue_h2d(i):
                 b = i % NB
-                for c, stream_c in enumerate(cs):
+                for ci, stream_c in enumerate(cs):
                     if i >= NB:
                         stream_c.wait_event(comp_done[i - NB])  # that step's compute has read these inputs
                     with torch.cuda.stream(stream_c):
-                        for n in names:
+                        for n in names_in:
                             if n in ("q", "scores"):
-                                r = rows_of(pin[n], c)
+                                r = rows_of(pin[n], ci)
                                 dsts[b][n][r].copy_(pin[n][r], non_blocking=True)
-                            elif c == 0:
+                            elif ci == 0:
                                 dsts[b][n].copy_(pin[n], non_blocking=True)
-                    h2d_done[i][c].record(stream_c)
+                    h2d_done[i][ci].record(stream_c)
 
             start, end = ev(), ev()
             start.record(cs[0])
@@ -421,16 +526,16 @@ def bench_ours(args):
                 b = i % NB
                 if i + 1 < nsteps:
                     issue_h2d(i + 1)
-                for c in range(len(cs)):
-                    stream.wait_event(h2d_done[i][c])
+                for ci in range(len(cs)):
+                    stream.wait_event(h2d_done[i][ci])
                 if i >= NB:
                     stream.wait_event(d2h_done[i - NB])  # that step's outputs have been read back
                 flush.zero_()
                 d = dsts[b]
-                sb = dict(bufs, out=outs[b], lse=lses[b])
+                sb = dict(bufs, out=outs[b], lse=lses[b], idx=idxs[b])
                 out, lse, _ = dsa.sparse_mla_topk(d["q"], inp.kv, inp.kv_scale, d["block_table"], d["q_req"],
                                                   d["q_pos"], d["scores"], w.k, num_splits=S, buffers=sb,
-                                                  dev_status=status, stream=stream, **kw)
+                                                  dev_status=status, stream=stream, fused=head["fused"], **kw)
                 comp_done[i].record(stream)
                 cs[0].wait_event(comp_done[i])
                 with torch.cuda.stream(cs[0]):
@@ -445,6 +550,8 @@ def bench_ours(args):
         barrier()
         e_ms = max_over_ranks(pipeline(args.steps), world, dev)
         # the pipelined results are the device-timed pass's, bit for bit
+        one_pass(dsa, head, stream, status)
+        torch.cuda.synchronize(dev)
         last = (args.steps - 1) % NB
         if not (torch.equal(out_h[last], bufs["out"].cpu()) and torch.equal(lse_h[last], bufs["lse"].cpu())):
             raise RuntimeError("end-to-end outputs differ from the device-timed pass")
@@ -453,8 +560,7 @@ def bench_ours(args):
                "note": "KV cache resident in HBM; every step copies its inputs (q, scores, q_pos, q_req, block "
                        "table) from pinned host memory and reads out + lse back inside the timed region; step "
                        "i+1's input copies overlap step i's compute (double buffers, copies split over "
-                       f"{len(cs)} copy streams); L2 "
-                       "flushed before every step's compute"}
+                       f"{len(cs)} copy streams); L2 flushed before every step's compute"}
     torch.cuda.synchronize(dev)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
@@ -483,11 +589,12 @@ def bench_ours(args):
             b.record(stream)
             b.synchronize()
             t_kvw.append(a.elapsed_time(b))
-        ms = statistics.mean(t_kvw)
+        ms = statistics.median(t_kvw)
         kbytes = n * (w.dqk * 2 + 4 + w.dqk + 4 + 4)  # rows read, req + pos read, codes + scale written
         kvw = {"rows": n, "ms": ms, "rows_per_s": n / (ms / 1e3), "algorithmic_bytes": kbytes,
-               "achieved_gbs": kbytes / (ms / 1e3) / 1e9, "bound": "hbm",
-               "note": "random distinct slots of the workload's pool; L2 flushed before every call"}
+               "achieved_gbs": kbytes / (ms / 1e3) / 1e9, "bound": "hbm", "peak_gbs": peaks["hbm_gbs"],
+               "frac": kbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+               "note": "random distinct slots of the workload's pool; L2 flushed before every call; median"}
         torch.cuda.synchronize(dev)
         assert int(status.item()) == 0, f"device status {int(status.item())}"
 
@@ -495,27 +602,6 @@ def bench_ours(args):
         if world > 1:
             torch.distributed.destroy_process_group()
         return 0
-
-    peaks = read_peaks()
-    if kvw:
-        kvw["peak_gbs"] = peaks["hbm_gbs"]
-        kvw["frac"] = kvw["achieved_gbs"] / peaks["hbm_gbs"]
-    fwd_ms = statistics.mean(t_fwd)
-    src = os.path.join(ROOT, "dsa_sparse_mla_topk_gb300", "csrc",
-                       "mla_tc.cu" if w.heads == 64 else "mla_simt.cu")
-    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
-    tr = TRAFFIC_BY_SOURCE.get(sha)
-    traffic = None
-    if tr and tr.get("workload") == w.name:
-        traffic = tr["bytes_per_launch"]
-    achieved_gbs = bytes_fwd / (fwd_ms / 1e3) / 1e9
-    ai_path = flops / bytes_path
-    ns_roof = min(NOMINAL_TFLOPS * 1e12, NOMINAL_GBS * 1e9 * ai_path)
-    achieved_flops = flops / (ms_per_step / 1e3)
-    meas_roof = min(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9 * ai_path)
-    # top-k (slices + merge for rows longer than 65,536 positions); the attention call
-    # (tensor-core path: resolve + attention kernels); combine when split
-    launches_per_step = (2 if topk_ws else 1) + (2 if ws_bytes else 1) + (1 if S > 1 else 0)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -527,24 +613,19 @@ def bench_ours(args):
                "sample": f"{n} of {w.num_q} query tokens (seeded), top-k + attention, fp64 C on all host cores",
                "seconds": secs}
 
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "e4m3" if src.endswith("mla_tc.cu") else "fp32",
+    line = {"metric": METRIC, "value": rep["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": rep["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic (seeded; shapes of the GLM-5.3-Flash workloads)",
-            "config": workload_config(w, S, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
-            "roofline": {"kernel": "sparse_mla_fwd", "bound": "hbm", "achieved": achieved_gbs,
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": traffic, "peak_source": peaks["source"],
-                         "algorithmic_bytes_per_launch": bytes_fwd, "avg_launch_ms": fwd_ms,
-                         "achieved_tflops": flops / (fwd_ms / 1e3) / 1e12},
-            "path_roofline": {"ai_flops_per_byte": ai_path, "achieved_tflops": achieved_flops / 1e12,
-                              "frac_nominal": achieved_flops / ns_roof, "frac_measured": achieved_flops / meas_roof,
-                              "nominal_roofline_tflops": ns_roof / 1e12},
-            "kernel_ms": {"topk": statistics.mean(t_topk), "sparse_mla_fwd": fwd_ms,
-                          "combine": statistics.mean(t_comb)},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-            "kv_write": kvw,
-            "clocks": sampler.summary() if sampler else None, "wall_s": wall}
+            "config": workload_config(w, S, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                             "path": rep["path"],
+                                             "timing": f"{rep['blocks']} blocks of exactly {args.steps} passes; "
+                                                       "value and ms_per_step from the median block"}),
+            "roofline": rep["roofline"], "path_roofline": rep["path_roofline"], "step_ms": rep["step_ms"],
+            "kernel_ms": rep["kernel_ms_separate_calls"], "attention_only": rep["attention_only"],
+            "workloads": reports, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": rep["gpu_launches_per_step"] * args.steps * rep["blocks"],
+            "kv_write": kvw, "clocks": sampler.summary() if sampler else None, "wall_s": wall}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

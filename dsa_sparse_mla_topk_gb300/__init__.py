@@ -14,7 +14,8 @@ import threading
 
 import torch
 
-__all__ = ["DsaError", "load_library", "topk_select", "sparse_mla_fwd", "combine", "sparse_mla_topk", "kv_write",
+__all__ = ["DsaError", "load_library", "topk_select", "sparse_mla_fwd", "combine", "sparse_mla_topk",
+           "sparse_mla_topk_fused", "use_fused_path", "kv_write",
            "PrefixCache",
            "kv_tile_count", "kv_tile_size", "pick_num_splits", "status_string", "EXPORTED_SYMBOLS",
            "DEV_BAD_QPOS", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT"]
@@ -27,6 +28,7 @@ DEV_BAD_QPOS, DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/dsa.h declares.
 EXPORTED_SYMBOLS = ("dsa_status_string", "dsa_version", "dsa_topk_select", "dsa_topk_workspace_size",
                     "dsa_sparse_mla_fwd", "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_fwd_noalloc",
+                    "dsa_sparse_mla_topk_fwd", "dsa_sparse_mla_topk_max_k",
                     "dsa_combine", "dsa_kv_write", "dsa_prefix_cache_create", "dsa_prefix_cache_destroy",
                     "dsa_prefix_cache_acquire", "dsa_prefix_cache_release", "dsa_prefix_cache_stats",
                     "dsa_kv_tile_count", "dsa_kv_tile_size", "dsa_pick_num_splits")
@@ -67,6 +69,11 @@ def load_library(path: str | None = None):
         lib.dsa_sparse_mla_fwd_noalloc.argtypes = [vp, vp, vp, i64, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32,
                                                    i32, f32, i32, vp, vp, vp, vp, vp, vp]
         lib.dsa_sparse_mla_fwd_noalloc.restype = i32
+        lib.dsa_sparse_mla_topk_fwd.argtypes = [vp, i64, vp, i32, vp, vp, vp, vp, i64, vp, i32, i32, vp, i32, i32, i32,
+                                                i32, i32, f32, vp, vp, vp, sz, vp, vp]
+        lib.dsa_sparse_mla_topk_fwd.restype = i32
+        lib.dsa_sparse_mla_topk_max_k.argtypes = []
+        lib.dsa_sparse_mla_topk_max_k.restype = i32
         lib.dsa_sparse_mla_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.dsa_sparse_mla_workspace_size.restype = sz
         lib.dsa_sparse_mla_fwd.restype = i32
@@ -308,16 +315,78 @@ class PrefixCache:
             pass
 
 
+def sparse_mla_topk_fused(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, *, d_latent: int,
+                          d_rope: int, page_size: int, softmax_scale: float, idx=None, out=None, lse=None,
+                          workspace=None, dev_status=None, stream=None):
+    """Top-k and the Partial step (one KV split) in one kernel call
+    (dsa_sparse_mla_topk_fwd); same results as topk_select followed by
+    sparse_mla_fwd.  Returns (out, lse, idx)."""
+    for t, name, dt in ((q, "q", torch.bfloat16), (kv, "kv", torch.uint8), (kv_scale, "kv_scale", torch.float32),
+                        (block_table, "block_table", torch.int32), (q_req, "q_req", torch.int32),
+                        (q_pos, "q_pos", torch.int32), (scores, "scores", torch.float32)):
+        _check(t, name, dt)
+    num_q, H, dqk = q.shape
+    if dqk != d_latent + d_rope or kv.shape[1] != dqk or kv.shape[0] % page_size:
+        raise ValueError("q / kv row sizes do not match d_latent + d_rope, or kv is not whole pages")
+    dev = q.device
+    if idx is None:
+        idx = torch.empty((num_q, k), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty((num_q, H, d_latent), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((num_q, H), dtype=torch.float32, device=dev)
+    ws_bytes = sparse_mla_workspace_size(num_q, H, d_latent, d_rope, k)
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _call("dsa_sparse_mla_topk_fwd", _p(scores), scores.shape[1], _p(q_pos), k, _p(idx), _p(q), _p(kv),
+          _p(kv_scale), kv.shape[0] // page_size, _p(block_table), block_table.shape[0], block_table.shape[1],
+          _p(q_req), num_q, H, d_latent, d_rope, page_size, float(softmax_scale), _p(out), _p(lse),
+          _p(workspace) if ws_bytes else None, ws_bytes, _p(dev_status), _stream(stream))
+    return out, lse, idx
+
+
+_SM_COUNT: dict = {}
+
+
+def use_fused_path(num_q: int, heads: int, d_latent: int, d_rope: int, ld: int, k: int, num_splits: int,
+                   device) -> bool:
+    """Whether sparse_mla_topk takes the single-kernel path: the tensor-core
+    shape, one KV split, rows of at most 65,536 positions, k within the
+    fused kernel's limit, and no more query tokens than SMs (decode).  With
+    more tokens the separate top-k kernel, which keeps two rows per SM in
+    flight, is faster."""
+    if (heads, d_latent, d_rope) != (64, 512, 64) or num_splits != 1 or ld > 65536:
+        return False
+    if k > load_library().dsa_sparse_mla_topk_max_k():
+        return False
+    dev = torch.device(device)
+    if dev not in _SM_COUNT:
+        _SM_COUNT[dev] = torch.cuda.get_device_properties(dev).multi_processor_count
+    return num_q <= _SM_COUNT[dev]
+
+
 def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, *, d_latent: int, d_rope: int,
                     page_size: int, softmax_scale: float, num_splits: int | None = None, buffers: dict | None = None,
-                    dev_status=None, stream=None):
+                    dev_status=None, stream=None, fused: bool | None = None):
     """One pass of the whole path: top-k -> Partial -> Combine (when split).
     ``buffers`` (optional) holds preallocated idx / out / lse / o_part /
-    lse_part / workspace tensors.  Returns (out, lse, idx)."""
+    lse_part / workspace tensors.  ``fused``: True runs top-k and the Partial
+    step in one kernel (dsa_sparse_mla_topk_fwd), False as separate calls,
+    None picks by use_fused_path (the same results either way).  Returns
+    (out, lse, idx)."""
     b = buffers or {}
     num_q, H, _ = q.shape
     if num_splits is None:
         num_splits = pick_num_splits(num_q, H, d_latent, d_rope, k)
+    if fused is None:
+        fused = use_fused_path(num_q, H, d_latent, d_rope, scores.shape[1], k, num_splits, q.device)
+    if fused:
+        if num_splits != 1:
+            raise ValueError("the fused path has one KV split")
+        return sparse_mla_topk_fused(q, kv, kv_scale, block_table, q_req, q_pos, scores, k, d_latent=d_latent,
+                                     d_rope=d_rope, page_size=page_size, softmax_scale=softmax_scale,
+                                     idx=b.get("idx"), out=b.get("out"), lse=b.get("lse"),
+                                     workspace=b.get("workspace"), dev_status=dev_status, stream=stream)
     idx = topk_select(scores, q_pos, k, idx=b.get("idx"), dev_status=dev_status, stream=stream,
                       workspace=b.get("topk_workspace"))
     if num_splits == 1:

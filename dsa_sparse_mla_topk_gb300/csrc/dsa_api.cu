@@ -183,6 +183,29 @@ dsa_status dsa_sparse_mla_fwd(const void* q, const uint8_t* kv, const float* kv_
   return from_cuda(dsa::launch_mla_simt(a, static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status dsa_sparse_mla_topk_fwd(const float* scores, int64_t ld_scores, const int32_t* q_pos, int32_t k,
+                                   int32_t* idx, const void* q, const uint8_t* kv, const float* kv_scale,
+                                   int64_t num_pages, const int32_t* block_table, int32_t num_req, int32_t bt_stride,
+                                   const int32_t* q_req, int32_t num_q, int32_t num_heads, int32_t d_latent,
+                                   int32_t d_rope, int32_t page_size, float softmax_scale, void* out, float* lse,
+                                   void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (ld_scores <= 0 || k <= 0 || num_q < 0) return DSA_ERR_INVALID_ARG;
+  if (!use_tensor_cores(num_heads, d_latent, d_rope)) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (ld_scores > 65536 || k > dsa::mla_tc_fused_max_k()) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (num_q == 0) return DSA_OK;
+  if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
+  dsa::MlaArgs a;
+  const size_t ws_need = dsa_sparse_mla_workspace_size(num_q, num_heads, d_latent, d_rope, k);
+  const dsa_status st = check_mla_args(q, kv, kv_scale, num_pages, block_table, num_req, bt_stride, q_req, idx,
+                                       num_q, num_heads, d_latent, d_rope, page_size, k, softmax_scale, 1, out, lse,
+                                       nullptr, nullptr, ws_need, workspace, workspace_bytes, dev_status, &a);
+  if (st != DSA_OK) return st;
+  return from_cuda(dsa::launch_mla_tc_fused(a, scores, ld_scores, q_pos, idx, workspace,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int32_t dsa_sparse_mla_topk_max_k(void) { return dsa::mla_tc_fused_max_k(); }
+
 // Test hook, not part of include/dsa.h: the fp32 CUDA-core kernel on any
 // supported shape, so that tests can cross-check it against the tensor-core
 // kernel on the 64-head shape.  Same arguments as dsa_sparse_mla_fwd minus

@@ -49,6 +49,12 @@ cudaError_t launch_mla_simt(const MlaArgs& a, cudaStream_t stream);
 bool mla_tc_supported(const MlaArgs& a);
 size_t mla_tc_workspace_bytes(int32_t num_q, int32_t k);
 cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream);
+// Fused decode path: top-k of each token's scores row, then attention over
+// it, one CTA per token (one KV split; rows of at most 65,536 positions; k at
+// most mla_tc_fused_max_k()); `workspace` as for launch_mla_tc.
+int mla_tc_fused_max_k();
+cudaError_t launch_mla_tc_fused(const MlaArgs& a, const float* scores, int64_t ld, const int32_t* q_pos, int32_t* idx,
+                                void* workspace, cudaStream_t stream);
 
 // KV cache write: FP8 E4M3 per-token quantisation + paged scatter (rows of up
 // to kv_write_max_d() values, a multiple of 16).

@@ -53,6 +53,7 @@
 
 #include "internal.cuh"
 #include "sm100_ptx.cuh"
+#include "topk_row.cuh"
 
 namespace dsa {
 namespace {
@@ -228,9 +229,37 @@ __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __r
   }
 }
 
+// The fused decode kernel's top-k inputs (unused by the plain kernel).
+struct TopkIn {
+  const float* scores;  // fp32 [num_q, ld]
+  int64_t ld;
+  const int32_t* q_pos;
+  int32_t* idx;         // output: int32 [num_q, k]
+};
+
+// The fused kernel selects its token's top k in KV stages 0 and 1 (candidate
+// keys, histogram, candidate positions, one bitmap) and the P buffer (the
+// other bitmap), all idle until the gathers start; the raw bf16 Q lands in
+// stages 2 and 3 meanwhile, and the Q region is free for its conversion.
+// The chosen positions overwrite the candidate keys once those are read.
+// The resolve step holds four entries per thread: k <= 2048.
+constexpr int FUSED_MAX_K = 4 * NTHREADS;
+static_assert(FUSED_MAX_K <= RLCAP, "the chosen positions fit where the candidate keys were");
+static_assert(sizeof(uint32_t) * (RLCAP + HBINS + RWORDS) + sizeof(uint16_t) * RLCAP == 2 * STAGE_BYTES,
+              "the top-k arrays but one bitmap fill KV stages 0 and 1");
+static_assert(sizeof(uint32_t) * RWORDS == 2 * P_BYTES, "the other bitmap fills the P buffer");
+static_assert(QSTAGE == 2, "the raw Q stays clear of the top-k arrays");
+static_assert(NTHREADS == RNT, "one CTA selects a row");
+
+// FUSED = false: attention over indices a previous top-k call chose, with
+// `res` filled by resolve_kernel.  FUSED = true (decode, one KV split): the
+// CTA first selects its own token's top k (the same selection the top-k
+// kernel makes), writes it to tk.idx and resolves it into `res`, then
+// attends to it: no kernel boundary and no wait for other tokens' rows.
+template <bool FUSED>
 __global__ void __launch_bounds__(NTHREADS, 1)
     mla_tc_kernel(const MlaArgs a, const __grid_constant__ CUtensorMap tmap_lat,
-                  const __grid_constant__ CUtensorMap tmap_rope, const int2* __restrict__ res) {
+                  const __grid_constant__ CUtensorMap tmap_rope, int2* __restrict__ res, const TopkIn tk) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* q_s = smem + OFF_Q;
@@ -257,6 +286,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int t_end = (int)((int64_t)ntiles * (split + 1) / S);
   const int ntl = t_end - t_begin;
   const int2* row_res = res + (int64_t)i * a.k;
+  // the fused kernel writes `res` itself, so it reads it back coherently
+  auto ld_res = [&](const int2* p) -> int2 {
+    if constexpr (FUSED) return __ldcg(p);
+    else return __ldg(p);
+  };
 
   if (ntl == 0) {  // an empty split: O = 0, lse = -inf
     for (int e = tid; e < H * DL; e += NTHREADS) {
@@ -310,6 +344,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  if (tid == 0) {  // raw Q into the staging stages, converted by all but the MMA warp
+    mbar_arrive_expect_tx(bar(B_QLOAD), 2 * STAGE_BYTES);
+    tma_bulk_load(smem_u32(smem + OFF_KV + QSTAGE * STAGE_BYTES),
+                  static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK, 2 * STAGE_BYTES, bar(B_QLOAD));
+  }
+
   const uint32_t kv_base = smem_u32(smem + OFF_KV), q_base = smem_u32(q_s), p_base = smem_u32(p_s);
   bool ok = true;
 
@@ -319,7 +359,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // (once the copies of tile 0 are out) and the softmax warps together: qt
   // numbers their NQ threads; named barrier 1 syncs them.
   constexpr int NQ = (NTMA + SOFTMAX_WARPS) * 32;
-  auto convert_q = [&](int qt) {
+  // qt numbers the nq participating threads; sync() is their barrier; with
+  // `arrive`, every participating warp arrives on B_QREADY at the end
+  auto convert_q_by = [&](int qt, int nq, auto sync, bool arrive) {
     constexpr int CH = DQK / 8;  // 16-byte chunks (8 bf16) per head
     const uint4* qraw = reinterpret_cast<const uint4*>(smem + OFF_KV + QSTAGE * STAGE_BYTES);
     auto bf_lo = [](uint32_t w) { return __uint_as_float(w << 16); };
@@ -327,7 +369,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (!wait_warp(B_QLOAD, 0)) ok = false;
     float mx = 0.f;
 #pragma unroll 4
-    for (int e = qt; e < H * CH; e += NQ) {
+    for (int e = qt; e < H * CH; e += nq) {
       const uint4 v = qraw[e];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -336,18 +378,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) red_s[qt >> 5] = mx;
-    named_barrier_sync(1, NQ);
+    sync();
     if (qt == 0) {
       float m = red_s[0];
-      for (int w = 1; w < NQ / 32; ++w) m = fmaxf(m, red_s[w]);
+      for (int w = 1; w < nq / 32; ++w) m = fmaxf(m, red_s[w]);
       int e = 0;
       if (m > 0.f && m <= 3.0e38f) frexpf(m, &e);  // m < 2^e
       *qexp_s = (m > 0.f && m <= 3.0e38f) ? 8 - e : 0;
     }
-    named_barrier_sync(1, NQ);
+    sync();
     const float qs = ldexpf(1.f, *qexp_s);
 #pragma unroll 4
-    for (int e = qt; e < H * CH; e += NQ) {
+    for (int e = qt; e < H * CH; e += nq) {
       const int h = e / CH, c = e % CH;
       const uint4 v = qraw[e];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -375,8 +417,79 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // warps' next copies into the staging stages and before the MMAs
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar(B_QREADY));
+    if (arrive && lane == 0) mbar_arrive(bar(B_QREADY));
   };
+  auto convert_q = [&](int qt) { convert_q_by(qt, NQ, [] { named_barrier_sync(1, NQ); }, true); };
+
+  if constexpr (FUSED) {
+    // ---------------- this token's top k, then its (slot, scale) pairs and Q ----------------
+    uint32_t* tk_small = reinterpret_cast<uint32_t*>(smem + OFF_RED);  // warp_buf[32] sel[4] minmax[2] wcount[16]
+    uint32_t* ckey = reinterpret_cast<uint32_t*>(smem + OFF_KV);
+    uint32_t* thist = ckey + RLCAP;
+    uint16_t* cpos = reinterpret_cast<uint16_t*>(thist + HBINS);
+    uint32_t* above_bm = reinterpret_cast<uint32_t*>(cpos + RLCAP);
+    uint32_t* equal_bm = reinterpret_cast<uint32_t*>(p_s);
+    int32_t* chosen = reinterpret_cast<int32_t*>(ckey);  // [k]: written after the candidates were read
+    const int64_t p = tk.q_pos[i];
+    const bool bad = p < 0 || p >= tk.ld;
+    const int vis = bad ? 0 : (int)(p + 1);
+    if (bad && tid == 0) report(a.dev_status, DSA_DEV_BAD_QPOS);
+    if (vis > a.k) {
+      row_select(tk.scores + (int64_t)i * tk.ld, vis, a.k, [&](uint32_t o, int32_t q) { chosen[o] = q; }, ckey, thist,
+                 above_bm, equal_bm, cpos, tk_small, tk_small + 32, tk_small + 36, tk_small + 38);
+    } else {
+      for (int j = tid; j < a.k; j += NTHREADS) chosen[j] = j < vis ? j : -1;
+    }
+    __syncthreads();
+    // Resolve four entries per thread at a time; the dependent loads (block
+    // table, then scale) overlap the two passes of the Q conversion.
+    const int32_t r = a.q_req[i];
+    const bool req_ok = r >= 0 && r < a.num_req;
+    constexpr int RPT = (FUSED_MAX_K + NTHREADS - 1) / NTHREADS;  // entries per thread at most
+    int32_t pos[RPT], page[RPT];
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+      const int j = tid + u * NTHREADS;
+      pos[u] = j < a.k ? chosen[j] : -1;
+      page[u] = -1;
+      if (pos[u] >= 0 && req_ok && pos[u] / a.page_size < a.bt_stride)
+        page[u] = __ldcg(&a.block_table[(int64_t)r * a.bt_stride + pos[u] / a.page_size]);
+    }
+    float sc[RPT];
+    int32_t slot[RPT];
+    bool issued_scales = false;
+    auto issue_scales = [&] {
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) {
+        slot[u] = -1;
+        sc[u] = 0.f;
+        if (pos[u] >= 0 && req_ok && pos[u] / a.page_size < a.bt_stride && page[u] >= 0 && page[u] < a.num_pages) {
+          slot[u] = page[u] * a.page_size + pos[u] % a.page_size;
+          sc[u] = __ldcg(&a.kv_scale[slot[u]]);
+        }
+      }
+      issued_scales = true;
+    };
+    // the Q conversion by all 16 warps, the scales' loads issued between its passes
+    convert_q_by(tid, NTHREADS, [&] {
+      if (!issued_scales) issue_scales();
+      __syncthreads();
+    }, false);
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+      const int j = tid + u * NTHREADS;
+      if (j >= a.k) continue;
+      if (pos[u] >= 0) {
+        if (!req_ok) report(a.dev_status, DSA_DEV_BAD_PAGE);
+        else if (pos[u] / a.page_size >= a.bt_stride) report(a.dev_status, DSA_DEV_BAD_INDEX);
+        else if (slot[u] < 0) report(a.dev_status, DSA_DEV_BAD_PAGE);
+      }
+      tk.idx[(int64_t)i * a.k + j] = pos[u];
+      res[(int64_t)i * a.k + j] = make_int2(slot[u], __float_as_int(sc[u]));
+    }
+    __syncthreads();  // `res` is complete, Q is converted, the top-k's shared memory is free again
+    if (tid == 0) mbar_arrive_count(bar(B_QREADY), NTMA + SOFTMAX_WARPS);
+  }
 
   if (warp < SOFTMAX_WARP0 && warp != WARP_MMA) {
     // ---------------- TMA warps: gather the selected rows, 4 per copy ----------------
@@ -385,11 +498,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int my_groups = (GROUPS - tw + NTMA - 1) / NTMA;
     const int g = tw + NTMA * lane;
     int issued = 0;
-    if (tw == 0 && lane == 0) {  // raw Q into the staging stages, converted by all but the MMA warp
-      mbar_arrive_expect_tx(bar(B_QLOAD), 2 * STAGE_BYTES);
-      tma_bulk_load(kv_base + QSTAGE * STAGE_BYTES, static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK,
-                    2 * STAGE_BYTES, bar(B_QLOAD));
-    }
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the resolve kernel's entries are complete
     for (int lt = 0; lt < ntl; ++lt) {
       const int s = lt % NST;
@@ -407,7 +515,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int base = (t_begin + lt) * T + 4 * g;
         int r[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) r[q] = base + q < a.k ? __ldg(&row_res[base + q].x) : -1;
+        for (int q = 0; q < 4; ++q) r[q] = base + q < a.k ? ld_res(&row_res[base + q]).x : -1;
         const int4 rows = make_int4(r[0], r[1], r[2], r[3]);
         const uint32_t dst = kv_base + s * STAGE_BYTES;
 #pragma unroll
@@ -416,7 +524,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_gather4(dst + ROPE_OFF + g * 256, &tmap_rope, DL, rows, bar(B_KVF + s));
       }
       issued = lt + 1;
-      if (lt == 0) convert_q(tw * 32 + lane);  // join the Q conversion once tile 0's copies are out
+      if (!FUSED && lt == 0) convert_q(tw * 32 + lane);  // join the Q conversion once tile 0's copies are out
     }
     // no copy may land after the CTA is gone: wait for the last ones (normally long complete)
     for (int lt = issued > NST ? issued - NST : 0; lt < issued; ++lt)
@@ -498,7 +606,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int hg = 2 * h2 + (lane >> 4);            // this thread's heads: [16 hg, 16 hg + 16)
     const int j = 16 * q4 + (lane & 15);            // this thread's tile row
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
-    convert_q(tid - SOFTMAX_WARP0 * 32 + NTMA * 32);
+    if (!FUSED) convert_q(tid - SOFTMAX_WARP0 * 32 + NTMA * 32);
     const float qk_scale = a.softmax_scale * LOG2E * ldexpf(1.f, -*qexp_s);
     // P' = p s_j 2^E with p <= 16: pick E so that 16 max_j s_j 2^E < 256,
     // max_j over the entries of this CTA's tiles
@@ -508,7 +616,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float sm = 0.f;
       const int e_end = t_end * T < a.k ? t_end * T : a.k;
       for (int e = t_begin * T + sw * 32 + lane; e < e_end; e += SOFTMAX_WARPS * 32)
-        sm = fmaxf(sm, __int_as_float(__ldg(&row_res[e].y)));
+        sm = fmaxf(sm, __int_as_float(ld_res(&row_res[e]).y));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, o));
       if (lane == 0) smax_s[sw] = sm;
@@ -537,7 +645,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     auto row_info = [&](int lt) -> int2 {
       const int e = (t_begin + lt) * T + j;
-      return e < a.k ? __ldg(row_res + e) : make_int2(-1, 0);
+      return e < a.k ? ld_res(row_res + e) : make_int2(-1, 0);
     };
     int2 info = row_info(0);
     for (int lt = 0; lt < ntl && ok; ++lt) {
@@ -805,7 +913,7 @@ cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream
   rcfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&rcfg, resolve_kernel, a, res);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  e = cudaFuncSetAttribute(mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the attention CTAs may start while the
   // resolve kernel runs; they wait for it (griddepcontrol.wait) before
@@ -817,8 +925,24 @@ cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mla_tc_kernel, a, map_lat, map_rope, static_cast<const int2*>(res));
+  e = cudaLaunchKernelEx(&cfg, mla_tc_kernel<false>, a, map_lat, map_rope, res, TopkIn{});
   if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+int mla_tc_fused_max_k() { return FUSED_MAX_K; }
+
+cudaError_t launch_mla_tc_fused(const MlaArgs& a, const float* scores, int64_t ld, const int32_t* q_pos, int32_t* idx,
+                                void* workspace, cudaStream_t stream) {
+  if (a.num_q == 0) return cudaSuccess;
+  if (a.num_splits != 1 || a.k > FUSED_MAX_K || ld > RMAXV) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap map_lat, map_rope;
+  if (!make_kv_map(&map_lat, a, 128, CU_TENSOR_MAP_SWIZZLE_128B) || !make_kv_map(&map_rope, a, DR, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const TopkIn tk{scores, ld, q_pos, idx};
+  mla_tc_kernel<true><<<a.num_q, NTHREADS, SMEM_BYTES, stream>>>(a, map_lat, map_rope, static_cast<int2*>(workspace), tk);
   return cudaGetLastError();
 }
 

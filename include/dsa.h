@@ -193,6 +193,36 @@ DSA_API dsa_status dsa_sparse_mla_fwd_noalloc(const void* q, const uint8_t* kv, 
                                               int32_t* dev_status, void* stream);
 
 /*
+ * dsa_sparse_mla_topk_fwd -- dsa_topk_select followed by dsa_sparse_mla_fwd
+ * with one KV split, in a single kernel: each CTA selects its own query
+ * token's top k and then attends to it.  Same results, bit for bit, as the
+ * two calls; [LMSYS] section 3 (the indexer's selection feeds the Partial
+ * step).  Meant for decode, where there are no more query tokens than SMs:
+ * the selection of one token's row no longer waits for every other row's,
+ * and no kernel boundary or index round trip through memory separates the
+ * two steps.  For many query tokens the separate calls are faster.
+ *
+ * Arguments are those of the two calls: scores, ld_scores, q_pos and k as
+ * for dsa_topk_select (ld_scores at most 65,536), idx is written as that call
+ * writes it, the rest as for dsa_sparse_mla_fwd with num_splits = 1 (out is
+ * required, lse may be NULL).  Only the tensor-core shape (64, 512, 64) and
+ * k <= dsa_sparse_mla_topk_max_k() are accepted; anything else returns
+ * DSA_ERR_UNSUPPORTED_SHAPE.  The workspace is dsa_sparse_mla_workspace_size()
+ * bytes.  A bad q_pos sets DSA_DEV_BAD_QPOS, gives a row of -1 and that
+ * token out = 0, lse = -inf.
+ */
+DSA_API dsa_status dsa_sparse_mla_topk_fwd(const float* scores, int64_t ld_scores, const int32_t* q_pos, int32_t k,
+                                           int32_t* idx, const void* q, const uint8_t* kv, const float* kv_scale,
+                                           int64_t num_pages, const int32_t* block_table, int32_t num_req,
+                                           int32_t bt_stride, const int32_t* q_req, int32_t num_q, int32_t num_heads,
+                                           int32_t d_latent, int32_t d_rope, int32_t page_size, float softmax_scale,
+                                           void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                           int32_t* dev_status, void* stream);
+
+/* Largest k dsa_sparse_mla_topk_fwd accepts. */
+DSA_API int32_t dsa_sparse_mla_topk_max_k(void);
+
+/*
  * dsa_combine -- the DSA "Combine" step: exact log-sum-exp merge of split-KV
  * partial results.  [LMSYS] section 3: KV splits add intermediate writes and
  * Combine work.

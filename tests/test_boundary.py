@@ -154,6 +154,31 @@ def test_combine_argument_checks(lib, args, expect):
     assert lib.dsa_combine(*args) == expect
 
 
+def _fused(lib, **over):
+    a = dict(scores=FAKE, ld=4096, qpos=FAKE, k=2048, idx=FAKE, q=FAKE, kv=FAKE, kv_scale=FAKE, num_pages=4, bt=FAKE,
+             num_req=1, bt_stride=4, q_req=FAKE, num_q=1, H=64, dl=512, dr=64, P=64, scale=0.04, out=FAKE, lse=FAKE,
+             ws=FAKE, wsb=1 << 20, st=None, stream=None)
+    a.update(over)
+    return lib.dsa_sparse_mla_topk_fwd(a["scores"], a["ld"], a["qpos"], a["k"], a["idx"], a["q"], a["kv"],
+                                       a["kv_scale"], a["num_pages"], a["bt"], a["num_req"], a["bt_stride"],
+                                       a["q_req"], a["num_q"], a["H"], a["dl"], a["dr"], a["P"], a["scale"], a["out"],
+                                       a["lse"], a["ws"], a["wsb"], a["st"], a["stream"])
+
+
+@no_device_only
+@pytest.mark.parametrize("over,expect", [
+    (dict(H=16, dl=64, dr=16), 2), (dict(ld=65537), 2), (dict(k=100000), 2), (dict(ld=0), 1), (dict(k=0), 1),
+    (dict(scores=None), 1), (dict(qpos=None), 1), (dict(idx=None), 1), (dict(out=None), 1), (dict(q=MISALIGNED), 1),
+    (dict(wsb=100), 3), (dict(num_q=0), 0),
+])
+def test_fused_argument_checks(lib, over, expect):
+    assert _fused(lib, **over) == expect
+
+
+def test_fused_max_k(lib):
+    assert lib.dsa_sparse_mla_topk_max_k() >= 2048
+
+
 def test_topk_workspace_size(lib):
     # (score, position) blocks of k per 65,536-position slice of every row
     assert dsa.topk_workspace_size(16, 1 << 20, 2048) == 16 * 16 * 2048 * 8

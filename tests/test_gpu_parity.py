@@ -485,3 +485,56 @@ def test_topk_long_rows_paths_and_large_k():
         assert (got[5] == -1).all()
         assert np.array_equal(got[:5], oracle.topk(sc.numpy()[:5], qp[:5], k))
     assert dsa.topk_workspace_size(6, ld, 20000) == 0  # 4 slices x 20000 > 65,536
+
+
+FUSED_CASES = [SMALL_H64, wl.DECODE_64K,
+               wl.Workload("fused_ties_h64", 5, 2, 64, 512, 64, 9001, 256, 64, 2048, seed=61, tie_frac=0.05,
+                           ctx_per_req=(9001, 8000, 2048, 2049, 300))]
+
+
+@pytest.mark.parametrize("w", FUSED_CASES, ids=lambda w: w.name)
+def test_fused_path_equals_separate_calls(w):
+    """dsa_sparse_mla_topk_fwd (top-k and attention in one kernel) must give
+    the indices, outputs and LSE of dsa_topk_select + dsa_sparse_mla_fwd bit
+    for bit: both run the same selection and the same attention pipeline."""
+    inp = inputs(w)
+    kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+    st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1, l1, i1 = dsa.sparse_mla_topk(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, inp.q_pos, inp.scores,
+                                     w.k, num_splits=1, fused=True, dev_status=st1, **kw)
+    o2, l2, i2 = dsa.sparse_mla_topk(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, inp.q_pos, inp.scores,
+                                     w.k, num_splits=1, fused=False, dev_status=st2, **kw)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == 0 and int(st2.item()) == 0
+    assert torch.equal(i1, i2)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # and the fused result against the oracle on a sample of tokens
+    rows = sample_rows(w.num_q, 24)
+    ref_idx, ref_out, ref_lse = oracle_rows(inp, rows)
+    assert np.array_equal(host(i1)[rows], ref_idx)
+    assert_close(host(o1.float())[rows], host(l1)[rows], ref_out, ref_lse, w.name + " fused")
+
+
+def test_fused_path_is_taken_for_decode_and_bad_rows_are_reported():
+    """The public pass picks the fused kernel for the decode workload, and a
+    query position outside the scores row gives BAD_QPOS, a row of -1 and an
+    empty attention (out 0, lse -inf) without faulting."""
+    w = SMALL_H64
+    assert dsa.use_fused_path(128, 64, 512, 64, 65536, 2048, 1, "cuda")
+    assert not dsa.use_fused_path(1024, 64, 512, 64, 65536, 2048, 1, "cuda")
+    assert not dsa.use_fused_path(16, 64, 512, 64, 1 << 20, 2048, 1, "cuda")
+    inp = inputs(w)
+    qp = inp.q_pos.clone()
+    qp[1] = inp.scores.shape[1] + 3
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse, idx = dsa.sparse_mla_topk_fused(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, qp, inp.scores,
+                                              w.k, d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size,
+                                              softmax_scale=w.scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & dsa.DEV_BAD_QPOS
+    assert bool((idx[1] == -1).all())
+    assert bool((out[1] == 0).all()) and bool(torch.isneginf(lse[1]).all())
+    ref = oracle.topk(host(inp.scores), host(inp.q_pos), w.k)
+    keep = [r for r in range(w.num_q) if r != 1]
+    assert np.array_equal(host(idx)[keep], ref[keep])
