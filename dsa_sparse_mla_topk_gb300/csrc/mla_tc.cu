@@ -810,8 +810,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // O^T (TMEM) -> normalised rows in the (now idle) KV stages, laid out
       // as the output [head][d], then one bulk copy to global memory: the
       // token's 64 x 512 result is contiguous (bf16, or fp32 for a split).
-      const float* inv = alpha_s + 32 * h2;
-      unsigned char* stg = smem + OFF_KV;
+      // O is staged as fp32 (full-word stores: a warp writes 128 contiguous
+      // bytes per instruction, where 16-bit stores were several times
+      // slower), then, for bf16 output, converted row-wise with 16-byte
+      // accesses into the Q region, which is idle by now.
+      // The 32 per-head factors go to registers first: read through a
+      // pointer the staging stores may alias, each would be reloaded after
+      // every store.
+      float inv[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) inv[h] = alpha_s[32 * h2 + h];
+      float* stg = reinterpret_cast<float*>(smem + OFF_KV);  // [head][d] fp32, 128 KB
 #pragma unroll 1
       for (int c = 0; c < NLAT; ++c) {
         const int d = 128 * c + 32 * q4 + lane;
@@ -821,16 +830,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tmem_ld16(t_lane + TM_O + 64 * c + 32 * h2 + 16 * g, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const int hh = 32 * h2 + 16 * g + h;
-            const float val = o[h] * inv[16 * g + h];
-            if (S == 1)
-              reinterpret_cast<__nv_bfloat16*>(stg)[hh * DL + d] = __float2bfloat16_rn(val);
-            else
-              reinterpret_cast<float*>(stg)[hh * DL + d] = val;
-          }
+          for (int h = 0; h < 16; ++h) stg[(32 * h2 + 16 * g + h) * DL + d] = o[h] * inv[16 * g + h];
         }
       }
+      named_barrier_sync(2, SOFTMAX_WARPS * 32);
+      unsigned char* src = reinterpret_cast<unsigned char*>(stg);
+      if (S == 1) {
+        uint4* ob = reinterpret_cast<uint4*>(q_s);  // [head][d] bf16, 64 KB
+        const float4* f4 = reinterpret_cast<const float4*>(stg);
+#pragma unroll 2
+        for (int e = sw * 32 + lane; e < H * DL / 8; e += SOFTMAX_WARPS * 32) {
+          const float4 x = f4[2 * e], y = f4[2 * e + 1];
+          const __nv_bfloat162 b0 = __floats2bfloat162_rn(x.x, x.y), b1 = __floats2bfloat162_rn(x.z, x.w);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(y.x, y.y), b3 = __floats2bfloat162_rn(y.z, y.w);
+          ob[e] = make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
+                             *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
+        }
+        src = q_s;
+        named_barrier_sync(2, SOFTMAX_WARPS * 32);
+      }
+      static_assert(H * DL * 4 <= NST * STAGE_BYTES && H * DL * 2 <= Q_BYTES, "O stages fit");
       fence_proxy_async_smem();
       named_barrier_sync(2, SOFTMAX_WARPS * 32);
       // 16 KB pieces, one per lane of softmax warp 0 (4 for bf16, 8 for fp32)
@@ -839,7 +858,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         unsigned char* dst = S == 1
                                  ? reinterpret_cast<unsigned char*>(static_cast<__nv_bfloat16*>(a.out) + (int64_t)i * H * DL)
                                  : reinterpret_cast<unsigned char*>(a.o_part + ((int64_t)split * a.num_q + i) * H * DL);
-        tma_bulk_store(dst + lane * piece, smem_u32(stg) + lane * piece, piece);
+        tma_bulk_store(dst + lane * piece, smem_u32(src) + lane * piece, piece);
         tma_bulk_store_wait_read();  // the shared memory stays valid until the copy has read it
       }
     } else if (lane == 0) {
