@@ -538,3 +538,27 @@ def test_fused_path_is_taken_for_decode_and_bad_rows_are_reported():
     ref = oracle.topk(host(inp.scores), host(inp.q_pos), w.k)
     keep = [r for r in range(w.num_q) if r != 1]
     assert np.array_equal(host(idx)[keep], ref[keep])
+
+
+def test_topk_many_rows_persistent_path_bit_exact():
+    """More rows than two CTAs per SM hold at once (several waves of the row
+    kernel): rows of every kind in one launch -- a bad query position, rows
+    shorter than k, heavy exact ties, an unaligned row stride -- must match
+    the oracle bit for bit."""
+    rng = np.random.default_rng(71)
+    n, ld, k = 700, 5003, 512
+    scores = rng.standard_normal((n, ld)).astype(np.float32)
+    scores[::7] = np.round(scores[::7] * 2)            # heavy ties on every 7th row
+    q_pos = rng.integers(0, ld, size=n).astype(np.int32)
+    q_pos[::11] = rng.integers(0, k, size=len(q_pos[::11]))  # rows shorter than k
+    q_pos[5] = ld + 9                                    # a bad query position
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = dsa.topk_select(torch.tensor(scores, device="cuda"), torch.tensor(q_pos, device="cuda"), k,
+                          dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == dsa.DEV_BAD_QPOS
+    ref = oracle.topk(scores, np.where(q_pos < ld, q_pos, 0).astype(np.int32), k)
+    g = host(got)
+    assert (g[5] == -1).all()
+    keep = np.arange(n) != 5
+    assert np.array_equal(g[keep], ref[keep])
