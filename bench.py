@@ -37,7 +37,12 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
 # capture, keyed by the SHA-1 of the kernel sources it was taken on (reported
 # as null once those sources change).
-TRAFFIC_BY_SOURCE: dict[str, dict] = {}
+TRAFFIC_BY_SOURCE: dict[str, dict] = {
+    # mla_tc.cu + topk_row.cuh: the fused decode kernel (top-k + attention)
+    "302a1720ca2269cb9ba2576bb24706c6cbb3f939": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_519_936},
+    # mla_tc.cu: the attention kernel as its own call
+    "58f49b03f324625283cf801c6b3225ecb0bf43fe": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49_558_272},
+}
 
 
 def parse_args():
