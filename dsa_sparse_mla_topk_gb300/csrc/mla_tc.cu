@@ -498,9 +498,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int my_groups = (GROUPS - tw + NTMA - 1) / NTMA;
     const int g = tw + NTMA * lane;
     int issued = 0;
+    // slots of tile rows 4g .. 4g + 3 of tile lt; loaded two tiles ahead, so
+    // that no L2 round trip sits between a stage's release and its next copies
+    auto load_rows = [&](int lt) -> int4 {
+      int r[4] = {-1, -1, -1, -1};
+      if (g < GROUPS && lt < ntl) {
+        const int base = (t_begin + lt) * T + 4 * g;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) r[q] = base + q < a.k ? ld_res(&row_res[base + q]).x : -1;
+      }
+      return make_int4(r[0], r[1], r[2], r[3]);
+    };
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the resolve kernel's entries are complete
+    int4 rows_cur = load_rows(0), rows_nxt = load_rows(1);
     for (int lt = 0; lt < ntl; ++lt) {
       const int s = lt % NST;
+      const int4 rows_far = load_rows(lt + 2);
       if (lt >= NST && !wait_warp(B_KVE + s, ((lt - NST) / NST) & 1)) {
         ok = false;
         break;
@@ -511,12 +524,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (lane == 0) mbar_arrive_expect_tx(bar(B_KVF + s), my_groups * (STAGE_BYTES / GROUPS));
       __syncwarp();
+      const int4 rows = rows_cur;
+      rows_cur = rows_nxt;
+      rows_nxt = rows_far;
       if (g < GROUPS) {  // tile rows 4g .. 4g + 3
-        const int base = (t_begin + lt) * T + 4 * g;
-        int r[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) r[q] = base + q < a.k ? ld_res(&row_res[base + q]).x : -1;
-        const int4 rows = make_int4(r[0], r[1], r[2], r[3]);
         const uint32_t dst = kv_base + s * STAGE_BYTES;
 #pragma unroll
         for (int ka = 0; ka < NLAT; ++ka)

@@ -48,9 +48,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Every wait on an mbarrier gives up after this much wall-clock time.
+constexpr uint64_t MBAR_LIMIT_NS = 2000000000ull;
+
 // Wait for the phase with the given parity to complete; false after
 // `limit_ns` of wall-clock time (the caller then reports a timeout).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = MBAR_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {

@@ -355,16 +355,34 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
       wcnt += __popc(b);
     }
   };
+  // A float4 per lane at a time: its four ballots first, then every
+  // candidate's slot from their counts (component-major within the warp's
+  // step; the list's order does not matter), stored without branches.
   auto screen = [&](const float4 (&v)[HB], int base) {
 #pragma unroll
     for (int d = 0; d < HB; ++d) {
       const int f = base + d * RNT + tid;
       const bool ok = f < nv4;
       const int e = h0 + 4 * f;
-      push(ok && v[d].x >= f_lo, v[d].x, e);
-      push(ok && v[d].y >= f_lo, v[d].y, e + 1);
-      push(ok && v[d].z >= f_lo, v[d].z, e + 2);
-      push(ok && v[d].w >= f_lo, v[d].w, e + 3);
+      const float x[4] = {v[d].x, v[d].y, v[d].z, v[d].w};
+      bool c[4];
+      uint32_t b[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        c[q] = ok && x[q] >= f_lo;
+        b[q] = __ballot_sync(0xffffffffu, c[q]);
+      }
+      uint32_t r = wcnt;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t slot = r + __popc(b[q] & lanes_below);
+        if (c[q] && slot < (uint32_t)RWCAP) {
+          wkey[slot] = __float_as_uint(x[q]);
+          wpos[slot] = (uint16_t)(e + q);
+        }
+        r += __popc(b[q]);
+      }
+      wcnt = r;
     }
   };
   // the loads of one half-batch are in flight while the other is screened
