@@ -295,8 +295,19 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
   const bool sampled = vis > RALL;
   const int blk = tid * SAMPLE_BLOCK;  // one sample block per thread covers a row
   float sv[SAMPLE_RUN];
+  static_assert(SAMPLE_RUN == 8 && SAMPLE_BLOCK % 4 == 0, "a sample run is two float4s");
+  if (sampled && head0 == 0 && blk + SAMPLE_RUN <= vis) {  // 16-byte aligned: two vector loads
+    const float4 u0 = __ldg(reinterpret_cast<const float4*>(s + blk));
+    const float4 u1 = __ldg(reinterpret_cast<const float4*>(s + blk) + 1);
+    sv[0] = u0.x, sv[1] = u0.y, sv[2] = u0.z, sv[3] = u0.w;
+    sv[4] = u1.x, sv[5] = u1.y, sv[6] = u1.z, sv[7] = u1.w;
+  } else {
 #pragma unroll
-  for (int t = 0; t < SAMPLE_RUN; ++t) sv[t] = sampled && blk + t < vis ? __ldg(s + blk + t) : 0.f;
+    for (int t = 0; t < SAMPLE_RUN; ++t) sv[t] = sampled && blk + t < vis ? __ldg(s + blk + t) : 0.f;
+  }
+  // the stream's first half-batch is in flight during the threshold step
+  float4 va[HB], vb[HB];
+  load(va, 0);
   if (tid < 8) {
     const uintptr_t a0 = (reinterpret_cast<uintptr_t>(s) + 15u) & ~uintptr_t(15);
     const uintptr_t a1 = reinterpret_cast<uintptr_t>(s + vis) & ~uintptr_t(15);
@@ -386,8 +397,6 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
     }
   };
   // the loads of one half-batch are in flight while the other is screened
-  float4 va[HB], vb[HB];
-  load(va, 0);
   for (int base = 0; base < nv4; base += 2 * RNT * HB) {
     load(vb, base + RNT * HB);
     screen(va, base);
