@@ -67,6 +67,9 @@ def parse_args():
     ap.add_argument("--copy-streams", type=int, default=2,
                     help="copy streams of the end-to-end leg; q and scores are split over them by rows")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--l2-flush", choices=["write", "clean"], default="write",
+                    help="before every timed step: write a 512 MiB buffer (write), or write it and then read a "
+                         "second 512 MiB buffer so that L2 holds no dirty lines (clean)")
     ap.add_argument("--kv-write-rows", type=int, default=32768,
                     help="rows of the separate KV-write measurement (0 = skip)")
     return ap.parse_args()
@@ -230,11 +233,11 @@ def host_copies(inp):
             "q_req": inp.q_req.cpu().numpy()}
 
 
-def workload_config(w, splits, extra=None):
+def workload_config(w, splits, extra=None, l2="flushed (512 MiB write) before every timed step"):
     cfg = {"workload": w.name, "requests": w.num_req, "query_tokens": w.num_q, "heads": w.heads,
            "d_latent": w.d_latent, "d_rope": w.d_rope, "context": w.ctx, "shared_prefix": w.shared_prefix,
            "page_size": w.page_size, "top_k": w.k, "kv_splits": splits, "kv_dtype": "fp8_e4m3+fp32 scale/token",
-           "l2": "flushed (512 MiB write) before every timed step"}
+           "l2": l2}
     if extra:
         cfg.update(extra)
     return cfg
@@ -332,6 +335,29 @@ def separate_calls(dsa, c, stream, status, evs):
     if S > 1:
         dsa.combine(bufs["o_part"], bufs["lse_part"], out=bufs["out"], lse=bufs["lse"], stream=stream)
     evs[3].record(stream)
+
+
+class L2Flush:
+    """Evicts the step's inputs from L2 before every timed step.  "write"
+    writes L2_FLUSH_BYTES; "clean" then also reads a second buffer of that
+    size, so that the lines left in L2 are clean and the timed step does not
+    pay for writing the flush's own data back to HBM."""
+
+    def __init__(self, torch, dev, mode):
+        self.torch, self.mode = torch, mode
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        if mode == "clean":
+            self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+            self.acc = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def describe(self):
+        return ("flushed (512 MiB write) before every timed step" if self.mode == "write" else
+                "flushed (512 MiB write, then a 512 MiB read: no dirty lines left) before every timed step")
+
+    def zero_(self):
+        self.w.zero_()
+        if self.mode == "clean":
+            self.torch.sum(self.r, 0, out=self.acc)
 
 
 def measure(dsa, c, args, torch, dev, stream, status, flush, world, barrier, peaks):
@@ -448,7 +474,7 @@ def bench_ours(args):
     names = [args.workload] + [n for n in args.also.split(",") if n and n != args.workload]
     stream = torch.cuda.current_stream(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev, args.l2_flush)
 
     def barrier():
         if world > 1:
@@ -622,7 +648,7 @@ def bench_ours(args):
             "warmup": args.warmup, "ms_per_step": rep["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic (seeded; shapes of the GLM-5.3-Flash workloads)",
-            "config": workload_config(w, S, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "config": workload_config(w, S, l2=flush.describe(), extra={"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                                              "path": rep["path"],
                                              "timing": f"{rep['blocks']} blocks of exactly {args.steps} passes; "
                                                        "value and ms_per_step from the median block"}),

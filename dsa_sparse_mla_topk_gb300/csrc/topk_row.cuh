@@ -178,8 +178,8 @@ __device__ void select_exact(const float* row_scores, const uint32_t* keys, cons
 // Rows of up to 65,536 visible positions: one CTA of 512 threads per row,
 // two CTAs per SM (80 KB of shared memory each), so that one CTA streams
 // while the other selects.
-//   0. The loads of a 1/16 sample (the first 8 of every 128 positions) are
-//      issued first, then an L2 bulk prefetch of the whole row.
+//   0. The loads of a 1/16 sample (the first 32 of every 512 positions: whole
+//      128-byte lines) are issued first, then an L2 bulk prefetch of the row.
 //   1. The sample places a lower 12-bit threshold T_lo as in the cluster
 //      kernel.
 //   2. One streaming pass screens every score against T_lo with one float
@@ -203,7 +203,10 @@ constexpr int RALL = 4096;               // rows this short take every position 
 constexpr int RDEPTH = 8;                // float4 loads in flight per thread
 constexpr int RWORDS = RMAXV / 32;       // bitmap words
 constexpr size_t RSMEM = sizeof(uint32_t) * (RLCAP + HBINS + 2 * RWORDS) + sizeof(uint16_t) * RLCAP;
-static_assert(RNT * SAMPLE_BLOCK == RMAXV, "one sample block per thread must cover a row");
+// The row's sample: the first RS_RUN positions of every RS_BLOCK (1/16),
+// whole 128-byte lines, eight positions per thread.
+constexpr int RS_BLOCK = 512, RS_RUN = 32;
+static_assert((RNT / (RS_RUN / 8)) * RS_BLOCK == RMAXV, "the threads' sample runs cover a row");
 
 __device__ __forceinline__ void l2_prefetch_bulk(uintptr_t addr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
@@ -289,21 +292,21 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
     }
   };
 
-  // ---- 0. loads in this order: a 1/16 sample (the first 8 of every 128
+  // ---- 0. loads in this order: a 1/16 sample (the first 32 of every 512
   // positions), then the whole row into L2 (eight 16-byte-aligned pieces
   // inside it) ----
   const bool sampled = vis > RALL;
-  const int blk = tid * SAMPLE_BLOCK;  // one sample block per thread covers a row
-  float sv[SAMPLE_RUN];
-  static_assert(SAMPLE_RUN == 8 && SAMPLE_BLOCK % 4 == 0, "a sample run is two float4s");
-  if (sampled && head0 == 0 && blk + SAMPLE_RUN <= vis) {  // 16-byte aligned: two vector loads
+  constexpr int SPT = 8;  // sampled positions per thread: two float4s
+  const int blk = (tid / (RS_RUN / SPT)) * RS_BLOCK + (tid % (RS_RUN / SPT)) * SPT;
+  float sv[SPT];
+  if (sampled && head0 == 0 && blk + SPT <= vis) {  // 16-byte aligned: two vector loads
     const float4 u0 = __ldg(reinterpret_cast<const float4*>(s + blk));
     const float4 u1 = __ldg(reinterpret_cast<const float4*>(s + blk) + 1);
     sv[0] = u0.x, sv[1] = u0.y, sv[2] = u0.z, sv[3] = u0.w;
     sv[4] = u1.x, sv[5] = u1.y, sv[6] = u1.z, sv[7] = u1.w;
   } else {
 #pragma unroll
-    for (int t = 0; t < SAMPLE_RUN; ++t) sv[t] = sampled && blk + t < vis ? __ldg(s + blk + t) : 0.f;
+    for (int t = 0; t < SPT; ++t) sv[t] = sampled && blk + t < vis ? __ldg(s + blk + t) : 0.f;
   }
   // the stream's first half-batch is in flight during the threshold step
   float4 va[HB], vb[HB];
@@ -330,9 +333,9 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
   uint32_t t_lo = 0u;
   if (sampled) {
 #pragma unroll
-    for (int t = 0; t < SAMPLE_RUN; ++t)
+    for (int t = 0; t < SPT; ++t)
       if (blk + t < vis) atomicAdd(&hist[score_key(sv[t]) >> 20], 1u);
-    const uint32_t ns = (uint32_t)(vis / SAMPLE_BLOCK) * SAMPLE_RUN + (uint32_t)min(vis % SAMPLE_BLOCK, SAMPLE_RUN);
+    const uint32_t ns = (uint32_t)(vis / RS_BLOCK) * RS_RUN + (uint32_t)min(vis % RS_BLOCK, RS_RUN);
     const float expect = (float)k * (float)ns / (float)vis;
     uint32_t need = (uint32_t)(expect * 1.25f) + 16u;
     if (need > ns) need = ns;

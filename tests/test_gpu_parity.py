@@ -355,15 +355,21 @@ def test_topk_sampling_fallbacks(ld):
     r2[(pos % 128) < 8] += 10.0                                            # sampled positions high
     rows.append(r2)
     rows.append(np.sort(np.random.default_rng(6).standard_normal(ld).astype(np.float32))[::-1].copy())
-    # the row kernel samples every 16th position
     r3 = np.random.default_rng(7).standard_normal(ld).astype(np.float32)
-    r3[(pos % 16) != 0] += 10.0                                            # unsampled positions high
+    r3[(pos % 16) != 0] += 10.0                                            # every 16th position low
     rows.append(r3)
     r4 = np.random.default_rng(8).standard_normal(ld).astype(np.float32)
-    r4[(pos % 16) == 0] += 10.0                                            # sampled positions high
+    r4[(pos % 16) == 0] += 10.0                                            # every 16th position high
     rows.append(r4)
+    # the row kernel samples the first 32 of every 512 positions
+    r5 = np.random.default_rng(9).standard_normal(ld).astype(np.float32)
+    r5[(pos % 512) >= 32] += 10.0                                          # unsampled positions high
+    rows.append(r5)
+    r6 = np.random.default_rng(10).standard_normal(ld).astype(np.float32)
+    r6[(pos % 512) < 32] += 10.0                                           # sampled positions high
+    rows.append(r6)
     scores = np.stack(rows)
-    q_pos = np.array([ld - 1, ld - 1, ld - 100, ld - 7, ld - 1, ld - 3], dtype=np.int32)
+    q_pos = np.array([ld - 1, ld - 1, ld - 100, ld - 7, ld - 1, ld - 3, ld - 1, ld - 2], dtype=np.int32)
     ref = oracle.topk(scores, q_pos, k)
     got = dsa.topk_select(torch.tensor(scores, device="cuda"), torch.tensor(q_pos, device="cuda"), k)
     assert np.array_equal(host(got), ref)
