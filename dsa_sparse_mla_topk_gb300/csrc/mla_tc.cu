@@ -388,9 +388,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     sync();
     const float qs = ldexpf(1.f, *qexp_s);
+    // chunk e = h CH + c, stepped by nq without a division per chunk
+    int h = qt / CH, c = qt % CH;
+    const int dh = nq / CH, dc = nq % CH;
 #pragma unroll 4
-    for (int e = qt; e < H * CH; e += nq) {
-      const int h = e / CH, c = e % CH;
+    for (int e = qt; e < H * CH; e += nq, h += dh, c += dc) {
+      if (c >= CH) c -= CH, ++h;
       const uint4 v = qraw[e];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t hi[4], lo[4];
@@ -431,6 +434,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t* equal_bm = reinterpret_cast<uint32_t*>(p_s);
     int32_t* chosen = reinterpret_cast<int32_t*>(ckey);  // [k]: written after the candidates were read
     const int64_t p = tk.q_pos[i];
+    const int32_t r = a.q_req[i];  // loaded now, used by the resolve after the selection
     const bool bad = p < 0 || p >= tk.ld;
     const int vis = bad ? 0 : (int)(p + 1);
     if (bad && tid == 0) report(a.dev_status, DSA_DEV_BAD_QPOS);
@@ -443,7 +447,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     // Resolve four entries per thread at a time; the dependent loads (block
     // table, then scale) overlap the two passes of the Q conversion.
-    const int32_t r = a.q_req[i];
     const bool req_ok = r >= 0 && r < a.num_req;
     constexpr int RPT = (FUSED_MAX_K + NTHREADS - 1) / NTHREADS;  // entries per thread at most
     int32_t pos[RPT], page[RPT];
