@@ -438,6 +438,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool bad = p < 0 || p >= tk.ld;
     const int vis = bad ? 0 : (int)(p + 1);
     if (bad && tid == 0) report(a.dev_status, DSA_DEV_BAD_QPOS);
+    // the request's block-table entries for the visible positions into L2,
+    // for the resolve after the selection (one warp, one line per lane)
+    if (warp == NTHREADS / 32 - 1 && r >= 0 && r < a.num_req && vis > 0) {
+      const int64_t nb = 4 * (int64_t)min(a.bt_stride, (vis + a.page_size - 1) / a.page_size);
+      const char* row = reinterpret_cast<const char*>(a.block_table + (int64_t)r * a.bt_stride);
+      for (int64_t off = lane * 128; off < nb; off += 32 * 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+      if (lane == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + nb - 1));  // an unaligned row's last line
+    }
     if (vis > a.k) {
       row_select(tk.scores + (int64_t)i * tk.ld, vis, a.k, [&](uint32_t o, int32_t q) { chosen[o] = q; }, ckey, thist,
                  above_bm, equal_bm, cpos, tk_small, tk_small + 32, tk_small + 36, tk_small + 38);
@@ -821,59 +829,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = group_sync(B_SYNCC, ph_c);
     }
     if (ok) {
-      // O^T (TMEM) -> normalised rows in the (now idle) KV stages, laid out
-      // as the output [head][d], then one bulk copy to global memory: the
-      // token's 64 x 512 result is contiguous (bf16, or fp32 for a split).
-      // O is staged as fp32 (full-word stores: a warp writes 128 contiguous
-      // bytes per instruction, where 16-bit stores were several times
-      // slower), then, for bf16 output, converted row-wise with 16-byte
-      // accesses into the Q region, which is idle by now.
-      // The 32 per-head factors go to registers first: read through a
-      // pointer the staging stores may alias, each would be reloaded after
-      // every store.
+      // O^T (TMEM) -> registers -> global memory: thread (q4, lane) holds
+      // latent dim d = 128 c + 32 q4 + lane of its 32 heads, so a warp's
+      // store covers 32 consecutive d of one head.  The 32 per-head factors
+      // go to registers first.
       float inv[32];
 #pragma unroll
       for (int h = 0; h < 32; ++h) inv[h] = alpha_s[32 * h2 + h];
-      float* stg = reinterpret_cast<float*>(smem + OFF_KV);  // [head][d] fp32, 128 KB
-#pragma unroll 1
-      for (int c = 0; c < NLAT; ++c) {
-        const int d = 128 * c + 32 * q4 + lane;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          float o[16];
-          tmem_ld16(t_lane + TM_O + 64 * c + 32 * h2 + 16 * g, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 16; ++h) stg[(32 * h2 + 16 * g + h) * DL + d] = o[h] * inv[16 * g + h];
-        }
-      }
-      named_barrier_sync(2, SOFTMAX_WARPS * 32);
-      unsigned char* src = reinterpret_cast<unsigned char*>(stg);
       if (S == 1) {
-        uint4* ob = reinterpret_cast<uint4*>(q_s);  // [head][d] bf16, 64 KB
-        const float4* f4 = reinterpret_cast<const float4*>(stg);
-#pragma unroll 2
-        for (int e = sw * 32 + lane; e < H * DL / 8; e += SOFTMAX_WARPS * 32) {
-          const float4 x = f4[2 * e], y = f4[2 * e + 1];
-          const __nv_bfloat162 b0 = __floats2bfloat162_rn(x.x, x.y), b1 = __floats2bfloat162_rn(x.z, x.w);
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(y.x, y.y), b3 = __floats2bfloat162_rn(y.z, y.w);
-          ob[e] = make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
-                             *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)i * H * DL + (int64_t)(32 * h2) * DL;
+#pragma unroll 1
+        for (int c = 0; c < NLAT; ++c) {
+          const int d = 128 * c + 32 * q4 + lane;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            float o[16];
+            tmem_ld16(t_lane + TM_O + 64 * c + 32 * h2 + 16 * g, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 16; ++h) ob[(16 * g + h) * DL + d] = __float2bfloat16_rn(o[h] * inv[16 * g + h]);
+          }
         }
-        src = q_s;
-        named_barrier_sync(2, SOFTMAX_WARPS * 32);
-      }
-      static_assert(H * DL * 4 <= NST * STAGE_BYTES && H * DL * 2 <= Q_BYTES, "O stages fit");
-      fence_proxy_async_smem();
-      named_barrier_sync(2, SOFTMAX_WARPS * 32);
-      // 16 KB pieces, one per lane of softmax warp 0 (4 for bf16, 8 for fp32)
-      const uint32_t piece = 16384, bytes = (uint32_t)(H * DL * (S == 1 ? 2 : 4));
-      if (sw == 0 && lane * piece < bytes) {
-        unsigned char* dst = S == 1
-                                 ? reinterpret_cast<unsigned char*>(static_cast<__nv_bfloat16*>(a.out) + (int64_t)i * H * DL)
-                                 : reinterpret_cast<unsigned char*>(a.o_part + ((int64_t)split * a.num_q + i) * H * DL);
-        tma_bulk_store(dst + lane * piece, smem_u32(src) + lane * piece, piece);
-        tma_bulk_store_wait_read();  // the shared memory stays valid until the copy has read it
+      } else {
+        float* op = a.o_part + ((int64_t)split * a.num_q + i) * H * DL + (int64_t)(32 * h2) * DL;
+#pragma unroll 1
+        for (int c = 0; c < NLAT; ++c) {
+          const int d = 128 * c + 32 * q4 + lane;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            float o[16];
+            tmem_ld16(t_lane + TM_O + 64 * c + 32 * h2 + 16 * g, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 16; ++h) op[(16 * g + h) * DL + d] = o[h] * inv[16 * g + h];
+          }
+        }
       }
     } else if (lane == 0) {
       report(a.dev_status, DSA_DEV_TIMEOUT);
