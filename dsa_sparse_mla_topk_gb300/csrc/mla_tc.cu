@@ -424,6 +424,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   };
   auto convert_q = [&](int qt) { convert_q_by(qt, NQ, [] { named_barrier_sync(1, NQ); }, true); };
 
+  // TMA warps: warp tw's lane l copies row group tw + NTMA l (tile rows
+  // 4g .. 4g + 3) of a tile, 4 rows per copy
+  const int tw = warp < WARP_MMA ? warp : warp - 1;
+  const int my_groups = (GROUPS - tw + NTMA - 1) / NTMA;
+  const int g = tw + NTMA * lane;
+  // the slots of this lane's row group of tile lt (-1: past k, read as zeros)
+  auto tile_rows = [&](int lt) -> int4 {
+    int r4[4] = {-1, -1, -1, -1};
+    if (g < GROUPS && lt < ntl) {
+      const int base = (t_begin + lt) * T + 4 * g;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) r4[q] = base + q < a.k ? ld_res(&row_res[base + q]).x : -1;
+    }
+    return make_int4(r4[0], r4[1], r4[2], r4[3]);
+  };
+  auto gather_tile = [&](int s, int4 rows) {  // a tile's rows into stage s (whole TMA warp)
+    if (lane == 0) mbar_arrive_expect_tx(bar(B_KVF + s), my_groups * (STAGE_BYTES / GROUPS));
+    __syncwarp();
+    if (g < GROUPS) {
+      const uint32_t dst = kv_base + s * STAGE_BYTES;
+#pragma unroll
+      for (int ka = 0; ka < NLAT; ++ka)
+        tma_gather4(dst + ka * LAT_BYTES + g * 512, &tmap_lat, ka * 128, rows, bar(B_KVF + s));
+      tma_gather4(dst + ROPE_OFF + g * 256, &tmap_rope, DL, rows, bar(B_KVF + s));
+    }
+  };
+
   if constexpr (FUSED) {
     // ---------------- this token's top k, then its (slot, scale) pairs and Q ----------------
     uint32_t* tk_small = reinterpret_cast<uint32_t*>(smem + OFF_RED);  // warp_buf[32] sel[4] minmax[2] wcount[16]
@@ -504,27 +531,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp < SOFTMAX_WARP0 && warp != WARP_MMA) {
     // ---------------- TMA warps: gather the selected rows, 4 per copy ----------------
-    // warp tw copies row groups tw, tw + NTMA, ... (lane l: group tw + NTMA l)
-    const int tw = warp < WARP_MMA ? warp : warp - 1;
-    const int my_groups = (GROUPS - tw + NTMA - 1) / NTMA;
-    const int g = tw + NTMA * lane;
+    // (the slots of the tile two ahead are loaded early, so that no L2 round
+    // trip sits between a stage's release and its next copies)
     int issued = 0;
-    // slots of tile rows 4g .. 4g + 3 of tile lt; loaded two tiles ahead, so
-    // that no L2 round trip sits between a stage's release and its next copies
-    auto load_rows = [&](int lt) -> int4 {
-      int r[4] = {-1, -1, -1, -1};
-      if (g < GROUPS && lt < ntl) {
-        const int base = (t_begin + lt) * T + 4 * g;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) r[q] = base + q < a.k ? ld_res(&row_res[base + q]).x : -1;
-      }
-      return make_int4(r[0], r[1], r[2], r[3]);
-    };
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the resolve kernel's entries are complete
-    int4 rows_cur = load_rows(0), rows_nxt = load_rows(1);
+    int4 rows_cur = tile_rows(0), rows_nxt = tile_rows(1);
     for (int lt = 0; lt < ntl; ++lt) {
       const int s = lt % NST;
-      const int4 rows_far = load_rows(lt + 2);
+      const int4 rows_far = tile_rows(lt + 2);
       if (lt >= NST && !wait_warp(B_KVE + s, ((lt - NST) / NST) & 1)) {
         ok = false;
         break;
@@ -533,18 +547,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = false;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(bar(B_KVF + s), my_groups * (STAGE_BYTES / GROUPS));
-      __syncwarp();
-      const int4 rows = rows_cur;
+      gather_tile(s, rows_cur);
       rows_cur = rows_nxt;
       rows_nxt = rows_far;
-      if (g < GROUPS) {  // tile rows 4g .. 4g + 3
-        const uint32_t dst = kv_base + s * STAGE_BYTES;
-#pragma unroll
-        for (int ka = 0; ka < NLAT; ++ka)
-          tma_gather4(dst + ka * LAT_BYTES + g * 512, &tmap_lat, ka * 128, rows, bar(B_KVF + s));
-        tma_gather4(dst + ROPE_OFF + g * 256, &tmap_rope, DL, rows, bar(B_KVF + s));
-      }
       issued = lt + 1;
       if (!FUSED && lt == 0) convert_q(tw * 32 + lane);  // join the Q conversion once tile 0's copies are out
     }
