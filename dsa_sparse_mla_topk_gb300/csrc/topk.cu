@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(RNT, 2)
   // the next kernel on the stream may be scheduled now; it waits for this
   // grid's results before reading them
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int64_t row = MODE == ROW_SLICE ? blockIdx.x / nslices : blockIdx.x;
   const int64_t p = q_pos[row];
   const bool bad = p < 0 || p >= ld;
