@@ -39,9 +39,9 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # as null once those sources change).
 TRAFFIC_BY_SOURCE: dict[str, dict] = {
     # mla_tc.cu + topk_row.cuh: the fused decode kernel (top-k + attention)
-    "302a1720ca2269cb9ba2576bb24706c6cbb3f939": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_519_936},
+    "5da56eb6df6b2d7f7009feb7d919b4eca3fc1879": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_563_712},
     # mla_tc.cu: the attention kernel as its own call
-    "58f49b03f324625283cf801c6b3225ecb0bf43fe": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49_558_272},
+    "e2dfd3622d46c50822358a030980bd8b8903814c": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49_710_592},
 }
 
 
