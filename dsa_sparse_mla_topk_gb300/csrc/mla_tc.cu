@@ -39,9 +39,13 @@
 //    P V of tile t-1 has read P(t-1).  All hand-offs are
 //    mbarriers; every wait is bounded in time and reports DSA_DEV_TIMEOUT
 //    instead of hanging.
+//  * The epilogue reads O^T from TMEM and stores it, normalised, straight to
+//    global memory (bf16 output, or the fp32 partial of a KV split).
 //  * A small resolve kernel first turns every selected position into its
 //    (slot, scale) pair, fully in parallel, into caller-provided scratch;
 //    the attention kernel is its programmatic dependent and overlaps it.
+//    The fused decode variant selects its token's top k, resolves it and
+//    converts Q in its own prologue instead.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -112,7 +116,6 @@ constexpr int B_QLOAD = B_QREADY + 1;     // raw bf16 Q has landed in the stagin
 constexpr int NBAR = B_QLOAD + 1;
 constexpr int QSTAGE = NST - 2;           // raw bf16 Q is staged in KV stages NST - 2 and NST - 1
 static_assert(2 * STAGE_BYTES == H * DQK * 2, "bf16 Q fills two KV stages");
-static_assert(NST * STAGE_BYTES >= H * DL * 4, "the epilogue stages O (fp32 partials) in the KV stages");
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_TMEM + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack

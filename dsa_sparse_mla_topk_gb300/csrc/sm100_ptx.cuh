@@ -87,18 +87,6 @@ __device__ __forceinline__ void tma_bulk_load(uint32_t dst, const void* src, uin
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
-// Contiguous bytes shared -> global (both 16-byte aligned, size a multiple of
-// 16), as one bulk-async group of this thread.
-__device__ __forceinline__ void tma_bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until every bulk-async group of this thread has finished reading its
-// shared-memory source.
-__device__ __forceinline__ void tma_bulk_store_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 __device__ __forceinline__ void tma_prefetch_map(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

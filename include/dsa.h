@@ -79,9 +79,8 @@ DSA_API int32_t dsa_version(void);
 
 /*
  * dsa_topk_select -- causal top-k over fp32 indexer scores.
- * [LMSYS] section 3: "the indexer selects KV positions" that the Partial step
- * then loads; [LMSYS] section 1: the indexer picks relevant historical
- * positions.
+ * [LMSYS] section 3: the Partial step loads the KV positions the indexer
+ * chose; [LMSYS] section 1: the indexer picks relevant historical positions.
  *
  * For each query row i (0 <= i < num_q) the visible positions are
  * 0..q_pos[i] (causal).  The call writes idx[i, 0:k] (int32, row-major,
