@@ -495,7 +495,10 @@ def test_topk_long_rows_paths_and_large_k():
 
 FUSED_CASES = [SMALL_H64, wl.DECODE_64K,
                wl.Workload("fused_ties_h64", 5, 2, 64, 512, 64, 9001, 256, 64, 2048, seed=61, tie_frac=0.05,
-                           ctx_per_req=(9001, 8000, 2048, 2049, 300))]
+                           ctx_per_req=(9001, 8000, 2048, 2049, 300)),
+               # k not a multiple of the 64-row tile; contexts below, at and just above k
+               wl.Workload("fused_k1000_h64", 5, 1, 64, 512, 64, 6000, 0, 64, 1000, seed=62,
+                           ctx_per_req=(6000, 999, 1000, 1001, 4321))]
 
 
 @pytest.mark.parametrize("w", FUSED_CASES, ids=lambda w: w.name)
