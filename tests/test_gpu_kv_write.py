@@ -123,3 +123,46 @@ def test_written_pool_feeds_the_attention_path():
     assert float(np.abs(got - ref_out).max()) <= 1e-2
     assert float(np.linalg.norm(got - ref_out) / np.linalg.norm(ref_out)) <= 5e-3
     assert float(np.abs(lse.cpu().numpy() - ref_lse).max()) <= 1e-3
+
+
+def test_kv_write_every_bf16_value_under_many_row_maxima():
+    """Every finite bf16 value x is quantised under row maxima a >= |x| from
+    every binade (three mantissas each, and three subnormal maxima): the
+    codes and scales must equal the oracle's, whose divisions are IEEE fp32.
+    This covers the kernel's reciprocal-and-correction quotient and its
+    division fallback for tiny maxima, at the boundaries where either could
+    round differently."""
+    d, page = 576, 64
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    finite = np.isfinite(vals)
+    maxima = [(e << 7) | m for e in range(1, 255) for m in (0x00, 0x45, 0x7F)] + [0x0001, 0x0040, 0x007F]
+    rows = []
+    for ab in maxima:
+        a = np.float32((np.uint32(ab) << 16).view(np.float32))
+        xs = bits[finite & (np.abs(vals) <= a)].astype(np.uint16)
+        per = d - 1
+        for s in range(0, len(xs), per):
+            row = np.full(d, ab, dtype=np.uint16)  # the row's maximum first, and as padding
+            chunk = xs[s:s + per]
+            row[1:1 + len(chunk)] = chunk
+            rows.append(row)
+    x_bits = np.stack(rows)
+    n = x_bits.shape[0]
+    pages = (n + page - 1) // page
+    bt = torch.arange(pages, dtype=torch.int32)[None, :]
+    req = torch.zeros(n, dtype=torch.int32)
+    pos = torch.arange(n, dtype=torch.int32)
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16)
+    kv = torch.zeros((pages * page, d), dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((pages * page,), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dsa.kv_write(x.cuda(), req.cuda(), pos.cuda(), bt.cuda(), kv, sc, page_size=page, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    kv_ref = np.zeros((pages * page, d), dtype=np.uint8)
+    sc_ref = np.zeros(pages * page, dtype=np.float32)
+    assert oracle.kv_write(x_bits.view(np.int16), req.numpy(), pos.numpy(), bt.numpy(), kv_ref, sc_ref,
+                           page_size=page) == oracle.OK
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), sc_ref.view(np.uint32))
+    assert np.array_equal(kv.cpu().numpy(), kv_ref)
