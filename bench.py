@@ -39,9 +39,9 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # as null once those sources change).
 TRAFFIC_BY_SOURCE: dict[str, dict] = {
     # mla_tc.cu + topk_row.cuh: the fused decode kernel (top-k + attention)
-    "5da56eb6df6b2d7f7009feb7d919b4eca3fc1879": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_563_712},
+    "79ce205c8dcb08014efef3a259bc623027d85f59": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_780_544},
     # mla_tc.cu: the attention kernel as its own call
-    "e2dfd3622d46c50822358a030980bd8b8903814c": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49_710_592},
+    "d3e55d0d30aa4b887df38f62455d07029eef0a0d": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49_920_256},
 }
 
 
