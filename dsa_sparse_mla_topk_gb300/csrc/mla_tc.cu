@@ -13,13 +13,16 @@
 //    Seven TMA warps gather the rows straight from the paged cache into
 //    shared memory with tile::gather4 (four arbitrary rows per copy; 128-byte
 //    swizzle for the 512 latent columns, 64-byte swizzle for the 64 rope
-//    columns; rows past the selection read as zeros); four tiles are in
+//    columns; rows past the selection read as zeros); five tiles are in
 //    flight and no thread touches KV bytes.
 //  * One MMA warp issues kind::f8f6f4 MMAs:
-//        S^T  = K [Q_hi | Q_lo]^T          M = 64 rows, N = 128, K = 576
+//        S    = [Q_hi ; Q_lo] K^T          M = 128 (64 heads hi, 64 lo), N = 64 rows, K = 576
 //        O^T += V^T P_hi^T + V^T P_lo^T    M = 4 x 128 latent dims, N = 64 heads, K = 64 rows
-//    V^T is the same shared-memory tile read MN-major.  Heads sit on N: one
-//    gathered row serves every head.
+//    The latent part of Q is the A operand straight from tensor memory (the
+//    MMA then reads only the 2 KB K slice from shared memory per step and
+//    runs at the tensor pipe's full rate); its rope part and K come from
+//    shared memory.  V^T is the same shared-memory tile read MN-major.  Every
+//    gathered row serves all 64 heads.
 //  * Q (bf16) and P (fp32) are carried as sums of two E4M3 numbers, hi =
 //    E4M3(x) and lo = E4M3(x - hi): about 8 significant bits, the precision
 //    of bf16.  Q is scaled by a power of two per query token so that its
@@ -29,14 +32,17 @@
 //  * The per-token dequantisation scale s_j multiplies the logits of row j
 //    and is folded into P before rounding (P'_hj = p_hj s_j 2^E), so V is used
 //    as the raw FP8 values.
-//  * 8 softmax warps (2 per TMEM lane quadrant) turn S into P; each thread
-//    owns one KV row and 16 heads.  Online softmax in the log2 domain with
-//    lazy rescaling: a head's reference max is raised (and O, l rescaled)
-//    only when a logit exceeds it by more than 2^4, so p <= 16 always.
-//  * TMEM holds two S^T buffers (2 x 128 columns) and O^T (4 x 64 columns);
-//    shared memory holds one P buffer.  QK^T of tile t+1 and the softmax of
-//    tile t run while P V of tile t-1 finishes; the softmax writes P(t) once
-//    P V of tile t-1 has read P(t-1).  All hand-offs are
+//  * 8 softmax warps (2 per TMEM lane quadrant) turn S into P.  Lane quadrant
+//    q holds heads 16 q .. 16 q + 15: Q_hi rows in its lanes 0-15, Q_lo rows
+//    in lanes 16-31, so one shuffle adds the two halves of a logit; each
+//    thread then owns one head and 16 rows of a tile.  Online softmax in the
+//    log2 domain with lazy rescaling: a head's reference max is raised (and
+//    O, l rescaled) only when a logit exceeds it by more than 2^4, so
+//    p <= 16 always.
+//  * TMEM holds two S buffers (2 x 64 columns), Q's latent A operand (128
+//    columns) and O^T (4 x 64 columns); shared memory holds two P buffers.
+//    QK^T runs two tiles ahead of P V: QK^T of tile t+2 is issued right after
+//    P V of tile t, while the softmax of tile t+1 runs.  All hand-offs are
 //    mbarriers; every wait is bounded in time and reports DSA_DEV_TIMEOUT
 //    instead of hanging.
 //  * The epilogue reads O^T from TMEM and stores it, normalised, straight to
@@ -66,16 +72,15 @@ using namespace sm100;
 
 constexpr int H = 64, DL = 512, DR = 64, DQK = DL + DR;
 constexpr int T = 64;                            // KV rows per tile
-constexpr int NST = 4;                           // KV tiles in flight
+constexpr int NST = 5;                           // KV tiles in flight
 constexpr int NLAT = DL / 128;                   // 128-column latent slices per row: 4
 constexpr int LAT_BYTES = T * 128;               // one latent slice of a tile (128-byte swizzle)
 constexpr int ROPE_OFF = NLAT * LAT_BYTES;       // the rope slice (64-byte swizzle)
 constexpr int STAGE_BYTES = ROPE_OFF + T * DR;   // 36 KB per tile
-constexpr int QN = 2 * H;                        // B rows of Q K^T: Q_hi heads, then Q_lo heads
-constexpr int QLAT_BYTES = QN * 128;
-constexpr int QROPE_OFF = NLAT * QLAT_BYTES;
-constexpr int Q_BYTES = QROPE_OFF + QN * DR;     // 72 KB
-constexpr int P_BYTES = T * H;                   // P_hi (or P_lo) of a tile: [row][head], 64-byte swizzle
+constexpr int QM = 2 * H;                        // A rows of Q K^T: Q_hi and Q_lo of every head
+constexpr int QROPE_BYTES = QM * DR;             // Q's rope part in shared memory (64-byte swizzle)
+constexpr int P_BYTES = H * T;                   // P_hi (or P_lo) of a tile: [head][row], K-major, 64-byte swizzle
+constexpr int NPB = 2;                           // P buffers
 constexpr int NTHREADS = 512;
 // Warp roles: 0-3 and 5-7 gather (a single CTA's TMA throughput grows with
 // the number of warps issuing copies), 4 issues the MMAs, 8-15 run the
@@ -87,26 +92,29 @@ constexpr float EXCEED_LOG2 = 4.0f;              // p = 2^(z - m) <= 2^4
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-// TMEM columns: S^T of buffer b at TM_S + 128 b (an M = 64 accumulator: tile
-// row r in lane 32 (r / 16) + r % 16; columns [0, 64) against Q_hi, [64, 128)
-// against Q_lo), O^T chunk c at TM_O + 64 c (M = 128: latent dim 128 c + lane).
-constexpr uint32_t TM_S = 0, TM_O = 256, TM_COLS = 512;
+// TMEM columns: S of buffer b at TM_S + 64 b (M = 128: lane = Q row, column =
+// tile row), Q's latent A operand at TM_Q (128 columns, 4 bytes of K each),
+// O^T chunk c at TM_O + 64 c (M = 128: latent dim 128 c + lane, column = head).
+// Q row (= lane) of head h: 32 (h / 16) + h % 16 for Q_hi, 16 more for Q_lo.
+constexpr uint32_t TM_S = 0, TM_Q = 2 * T, TM_O = 256, TM_COLS = 512;
+static_assert(TM_Q + DL / 4 == TM_O, "S, Q and O fill the 512 TMEM columns");
+__host__ __device__ constexpr int q_row(int h, int lo) { return 32 * (h >> 4) + (h & 15) + 16 * lo; }
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int OFF_KV = 0;
-constexpr int OFF_Q = OFF_KV + NST * STAGE_BYTES;
-constexpr int OFF_P = OFF_Q + Q_BYTES;               // [hi, lo]: one buffer
-constexpr int OFF_RED = OFF_P + 2 * P_BYTES;         // [4 quadrants][64 heads] floats
-constexpr int OFF_MUSE = OFF_RED + 4 * H * 4;        // reference max per head (log2 domain)
-constexpr int OFF_ALPHA = OFF_MUSE + H * 4;
-constexpr int OFF_FLAG = OFF_ALPHA + H * 4;          // votes [2][8], rescale flags [2], Q exponent
+constexpr int OFF_QR = OFF_KV + NST * STAGE_BYTES;   // Q rope rows (hi and lo)
+constexpr int OFF_P = OFF_QR + QROPE_BYTES;          // [buffer][hi, lo]
+constexpr int OFF_RED = OFF_P + NPB * 2 * P_BYTES;   // [4][64] floats: reductions
+constexpr int OFF_ALPHA = OFF_RED + 4 * H * 4;       // per-head rescale factor, then 1 / l
+constexpr int OFF_ROWF = OFF_ALPHA + H * 4;          // [8 warps][2 tiles][32 rows] logit factor
+constexpr int OFF_FLAG = OFF_ROWF + SOFTMAX_WARPS * 2 * 32 * 4;  // votes [2][8], rescale flags [4], Q exponent, ...
 constexpr int OFF_BAR = OFF_FLAG + 128;
 constexpr int B_KVF = 0;                  // [NST] tile in stage s has landed (TMA transaction bytes)
 constexpr int B_KVE = B_KVF + NST;        // [NST] stage s is free (its P V MMAs are done)
-constexpr int B_SF = B_KVE + NST;         // [2] S^T buffer b is complete
-constexpr int B_PF = B_SF + 2;            // P of the next tile is written (and O rescaled)
-constexpr int B_PVD = B_PF + 1;           // P V of a tile is done (one phase per tile): P is free
-constexpr int B_OF = B_PVD + 1;           // every P V is done
+constexpr int B_SF = B_KVE + NST;         // [2] S buffer b is complete
+constexpr int B_PF = B_SF + 2;            // [2] P buffer b is written (and O rescaled)
+constexpr int B_PVD = B_PF + NPB;         // [2] P V of the tile in P buffer b is done: b is free
+constexpr int B_OF = B_PVD + NPB;         // every P V is done
 constexpr int B_SYNCA = B_OF + 1;         // softmax-group sync points
 constexpr int B_SYNCB = B_SYNCA + 1;
 constexpr int B_SYNCC = B_SYNCB + 1;
@@ -120,7 +128,7 @@ constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_TMEM + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
+static_assert(OFF_QR % 1024 == 0 && OFF_P % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -143,44 +151,6 @@ __device__ __forceinline__ void split_e4m3x2(uint32_t h2, uint32_t& hi, uint32_t
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float x0, float x1) {
   const __half2 h = __floats2half2_rn(x0, x1);  // x0 in the low half
   return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Per-half-warp transpose-reduction: v[16] per lane (16 heads) -> lane l
-// returns the reduction over the 16 lanes of its half of head l % 16.
-template <bool IS_MAX>
-__device__ __forceinline__ float half_warp_transpose_reduce(const float (&v)[16], int lane) {
-  float a8[8], a4[4], a2[2];
-  {
-    const bool up = lane & 8;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float send = up ? v[i] : v[i + 8], keep = up ? v[i + 8] : v[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, 8);
-      a8[i] = IS_MAX ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  {
-    const bool up = lane & 4;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float send = up ? a8[i] : a8[i + 4], keep = up ? a8[i + 4] : a8[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, 4);
-      a4[i] = IS_MAX ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  {
-    const bool up = lane & 2;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float send = up ? a4[i] : a4[i + 2], keep = up ? a4[i + 2] : a4[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, 2);
-      a2[i] = IS_MAX ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  const bool up = lane & 1;
-  const float send = up ? a2[0] : a2[1], keep = up ? a2[1] : a2[0];
-  const float got = __shfl_xor_sync(0xffffffffu, send, 1);
-  return IS_MAX ? fmaxf(keep, got) : keep + got;
 }
 
 // Resolve every selected position into (slot, dequantisation scale) once,
@@ -241,17 +211,17 @@ struct TopkIn {
 };
 
 // The fused kernel selects its token's top k in KV stages 0 and 1 (candidate
-// keys, histogram, candidate positions, one bitmap) and the P buffer (the
+// keys, histogram, candidate positions, one bitmap) and the P buffers (the
 // other bitmap), all idle until the gathers start; the raw bf16 Q lands in
-// stages 2 and 3 meanwhile, and the Q region is free for its conversion.
+// the last two stages meanwhile.
 // The chosen positions overwrite the candidate keys once those are read.
 // The resolve step holds four entries per thread: k <= 2048.
 constexpr int FUSED_MAX_K = 4 * NTHREADS;
 static_assert(FUSED_MAX_K <= RLCAP, "the chosen positions fit where the candidate keys were");
 static_assert(sizeof(uint32_t) * (RLCAP + HBINS + RWORDS) + sizeof(uint16_t) * RLCAP == 2 * STAGE_BYTES,
               "the top-k arrays but one bitmap fill KV stages 0 and 1");
-static_assert(sizeof(uint32_t) * RWORDS == 2 * P_BYTES, "the other bitmap fills the P buffer");
-static_assert(QSTAGE == 2, "the raw Q stays clear of the top-k arrays");
+static_assert(sizeof(uint32_t) * RWORDS <= NPB * 2 * P_BYTES, "the other bitmap fits in the P buffers");
+static_assert(QSTAGE >= 2, "the raw Q stays clear of the top-k arrays");
 static_assert(NTHREADS == RNT, "one CTA selects a row");
 
 // FUSED = false: attention over indices a previous top-k call chose, with
@@ -265,15 +235,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                   const __grid_constant__ CUtensorMap tmap_rope, int2* __restrict__ res, const TopkIn tk) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* q_s = smem + OFF_Q;
+  unsigned char* qr_s = smem + OFF_QR;
   unsigned char* p_s = smem + OFF_P;
   float* red_s = reinterpret_cast<float*>(smem + OFF_RED);
-  float* muse_s = reinterpret_cast<float*>(smem + OFF_MUSE);
   float* alpha_s = reinterpret_cast<float*>(smem + OFF_ALPHA);
   int* vote_s = reinterpret_cast<int*>(smem + OFF_FLAG);  // [2][8] per-tile votes (double buffered)
-  int* resc_s = vote_s + 16;                                // [2] rescale needed, per head half
-  int* qexp_s = vote_s + 18;                                // Q's power-of-two scale
-  float* smax_s = reinterpret_cast<float*>(vote_s + 20);   // [8] softmax warps' largest scales
+  int* resc_s = vote_s + 16;                                // [4] rescale needed, per lane quadrant
+  int* qexp_s = vote_s + 20;                                // Q's power-of-two scale
+  float* smax_s = reinterpret_cast<float*>(vote_s + 21);   // [8] softmax warps' largest scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
   auto bar = [&](int b) { return smem_u32(bars + b); };
@@ -323,14 +292,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_KVE + s), 1);
     }
     for (int b = 0; b < 2; ++b) mbar_init(bar(B_SF + b), 1);
-    mbar_init(bar(B_PF), SOFTMAX_WARPS);
-    mbar_init(bar(B_PVD), 1);
+    for (int b = 0; b < NPB; ++b) {
+      mbar_init(bar(B_PF + b), SOFTMAX_WARPS);
+      mbar_init(bar(B_PVD + b), 1);
+    }
     mbar_init(bar(B_OF), 1);
     mbar_init(bar(B_SYNCA), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCB), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCC), SOFTMAX_WARPS);
     mbar_init(bar(B_FIN), 1);
-    mbar_init(bar(B_QREADY), NTMA + SOFTMAX_WARPS);
+    mbar_init(bar(B_QREADY), NTHREADS / 32);
     mbar_init(bar(B_QLOAD), 1);
     fence_mbarrier_init();
   }
@@ -338,10 +309,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tma_prefetch_map(&tmap_lat);
     tma_prefetch_map(&tmap_rope);
   }
-  if (tid < H) {
-    muse_s[tid] = -INFINITY;
-    alpha_s[tid] = 1.f;
-  }
+  if (tid < H) alpha_s[tid] = 1.f;
 
   tc_fence_before_sync();
   __syncthreads();
@@ -353,17 +321,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                   static_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * H * DQK, 2 * STAGE_BYTES, bar(B_QLOAD));
   }
 
-  const uint32_t kv_base = smem_u32(smem + OFF_KV), q_base = smem_u32(q_s), p_base = smem_u32(p_s);
+  const uint32_t kv_base = smem_u32(smem + OFF_KV), qr_base = smem_u32(qr_s), p_base = smem_u32(p_s);
   bool ok = true;
 
   // Q of this token: bf16 [64 heads][576] (bulk-copied into the two staging
-  // KV stages) -> x 2^qexp -> E4M3 hi (B rows 0..63) and lo (B rows
-  // 64..127), K-major, in the MMA's swizzled layouts.  Done by the TMA warps
-  // (once the copies of tile 0 are out) and the softmax warps together: qt
-  // numbers their NQ threads; named barrier 1 syncs them.
-  constexpr int NQ = (NTMA + SOFTMAX_WARPS) * 32;
-  // qt numbers the nq participating threads; sync() is their barrier; with
-  // `arrive`, every participating warp arrives on B_QREADY at the end
+  // KV stages) -> x 2^qexp -> E4M3 hi and lo.  The latent part goes to TMEM
+  // (the QK^T A operand: row q_row(h, lo) in that lane, 4 bytes per column),
+  // written by the warps of the row's lane quadrant; the rope part goes to
+  // shared memory (K-major, 64-byte swizzle).  All 16 warps take part (the
+  // TMA warps once the copies of tile 0 are out): qt numbers the threads;
+  // sync() is their barrier; with `arrive`, every warp arrives on B_QREADY
+  // at the end.
   auto convert_q_by = [&](int qt, int nq, auto sync, bool arrive) {
     constexpr int CH = DQK / 8;  // 16-byte chunks (8 bf16) per head
     const uint4* qraw = reinterpret_cast<const uint4*>(smem + OFF_KV + QSTAGE * STAGE_BYTES);
@@ -391,41 +359,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     sync();
     const float qs = ldexpf(1.f, *qexp_s);
-    // chunk e = h CH + c, stepped by nq without a division per chunk
-    int h = qt / CH, c = qt % CH;
-    const int dh = nq / CH, dc = nq % CH;
-#pragma unroll 4
-    for (int e = qt; e < H * CH; e += nq, h += dh, c += dc) {
-      if (c >= CH) c -= CH, ++h;
-      const uint4 v = qraw[e];
+    // hi and lo of 8 elements (one 16-byte chunk of raw Q), as byte quadruples
+    auto split8 = [&](const uint4 v, uint2& hv, uint2& lv) {
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) split_e4m3x2(f32x2_to_f16x2(bf_lo(w[t]) * qs, bf_hi(w[t]) * qs), hi[t], lo[t]);
-      const uint2 hv = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
-      const uint2 lv = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
-      const int b = c * 8;  // byte column
-      uint32_t off_hi, off_lo;
-      if (b < DL) {
-        const int ka = b >> 7, cc = (b & 127) >> 4, half = (b >> 3) & 1;
-        const uint32_t in_row = ((cc ^ (h & 7)) << 4) + half * 8;  // row 64 + h has the same phase as h
-        off_hi = ka * QLAT_BYTES + h * 128 + in_row;
-        off_lo = ka * QLAT_BYTES + (H + h) * 128 + in_row;
-      } else {
-        const int br = b - DL, cc = br >> 4, half = (br >> 3) & 1;
-        off_hi = QROPE_OFF + h * 64 + ((cc ^ ((h >> 1) & 3)) << 4) + half * 8;
-        off_lo = QROPE_OFF + (H + h) * 64 + ((cc ^ (((H + h) >> 1) & 3)) << 4) + half * 8;
+      hv = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+      lv = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+    };
+    {
+      // latent: lane u of warp w (lane quadrant q4 = w % 4) writes row 32 q4 + u,
+      // i.e. Q_hi (u < 16) or Q_lo (u >= 16) of head 16 q4 + u % 16, 32-element
+      // column blocks j = w / 4, w / 4 + 4, ...  The two lanes of a head split
+      // each block's four 8-element chunks between them and swap halves.
+      const int q4 = warp & 3, h = 16 * q4 + (lane & 15), lo = lane >> 4;
+      const uint32_t t_q = tmem + ((uint32_t)(32 * q4) << 16) + TM_Q;
+      for (int j = warp >> 2; j < DL / 32; j += 4) {
+        // this lane splits chunks 2 lo and 2 lo + 1 of the block (loaded in an
+        // order that staggers the banks), keeps its half and swaps the other
+        const uint4* src = qraw + h * CH + 4 * j + 2 * lo;
+        const uint4 ra = src[lane & 1], rb = src[(lane & 1) ^ 1];
+        uint2 keep[2], recv[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          uint2 hv, lv;
+          split8((t ^ (lane & 1)) ? rb : ra, hv, lv);
+          keep[t] = lo ? lv : hv;
+          const uint2 send = lo ? hv : lv;
+          recv[t] = make_uint2(__shfl_xor_sync(0xffffffffu, send.x, 16), __shfl_xor_sync(0xffffffffu, send.y, 16));
+        }
+        const uint2 c0 = lo ? recv[0] : keep[0], c1 = lo ? recv[1] : keep[1];  // chunks 0, 1
+        const uint2 c2 = lo ? keep[0] : recv[0], c3 = lo ? keep[1] : recv[1];  // chunks 2, 3
+        const uint32_t col[8] = {c0.x, c0.y, c1.x, c1.y, c2.x, c2.y, c3.x, c3.y};
+        tmem_st8(t_q + 8 * j, col);
       }
-      *reinterpret_cast<uint2*>(q_s + off_hi) = hv;
-      *reinterpret_cast<uint2*>(q_s + off_lo) = lv;
+      tmem_wait_st();
+    }
+    // rope: 8 chunks of 8 elements per head
+    for (int e = qt; e < H * (DR / 8); e += nq) {
+      const int h = e >> 3, c = e & 7;
+      uint2 hv, lv;
+      split8(qraw[h * CH + DL / 8 + c], hv, lv);
+      const int cc = c >> 1, half = c & 1;  // 16-byte column and its half
+      const int rh = q_row(h, 0), rl = q_row(h, 1);
+      *reinterpret_cast<uint2*>(qr_s + rh * DR + ((cc ^ ((rh >> 1) & 3)) << 4) + half * 8) = hv;
+      *reinterpret_cast<uint2*>(qr_s + rl * DR + ((cc ^ ((rl >> 1) & 3)) << 4) + half * 8) = lv;
     }
     // the raw Q reads and the hi/lo writes are ordered before the TMA
     // warps' next copies into the staging stages and before the MMAs
     fence_proxy_async_smem();
+    tc_fence_before_sync();
     __syncwarp();
     if (arrive && lane == 0) mbar_arrive(bar(B_QREADY));
   };
-  auto convert_q = [&](int qt) { convert_q_by(qt, NQ, [] { named_barrier_sync(1, NQ); }, true); };
+  auto convert_q = [&](int qt) { convert_q_by(qt, NTHREADS, [] { named_barrier_sync(1, NTHREADS); }, true); };
 
   // TMA warps: warp tw's lane l copies row group tw + NTMA l (tile rows
   // 4g .. 4g + 3) of a tile, 4 rows per copy
@@ -529,7 +517,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       res[(int64_t)i * a.k + j] = make_int2(slot[u], __float_as_int(sc[u]));
     }
     __syncthreads();  // `res` is complete, Q is converted, the top-k's shared memory is free again
-    if (tid == 0) mbar_arrive_count(bar(B_QREADY), NTMA + SOFTMAX_WARPS);
+    if (tid == 0) mbar_arrive_count(bar(B_QREADY), NTHREADS / 32);
   }
 
   if (warp < SOFTMAX_WARP0 && warp != WARP_MMA) {
@@ -562,20 +550,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (!ok && lane == 0) report(a.dev_status, DSA_DEV_TIMEOUT);
   } else if (warp == WARP_MMA) {
     // ---------------- MMA warp ----------------
-    constexpr uint32_t ID_QK = idesc_f16_f32(64, QN, 0, 0, 0);   // kind::f8f6f4: E4M3 x E4M3 -> f32
-    constexpr uint32_t ID_PV = idesc_f16_f32(128, H, 1, 1, 0);
+    constexpr uint32_t ID_QK = idesc_f16_f32(QM, T, 0, 0, 0);  // kind::f8f6f4: E4M3 x E4M3 -> f32
+    constexpr uint32_t ID_PV = idesc_f16_f32(128, H, 1, 0, 0);
+    const uint64_t a_rope = smem_desc(qr_base, 16, 512, SWIZZLE_64B);
     auto issue_qk = [&](int lt) {
       const uint32_t stage = kv_base + (lt % NST) * STAGE_BYTES;
-      const uint64_t a_lat = smem_desc(stage, 16, 1024, SWIZZLE_128B);
-      const uint64_t a_rope = smem_desc(stage + ROPE_OFF, 16, 512, SWIZZLE_64B);
-      const uint64_t b_lat = smem_desc(q_base, 16, 1024, SWIZZLE_128B);
-      const uint64_t b_rope = smem_desc(q_base + QROPE_OFF, 16, 512, SWIZZLE_64B);
-      const uint32_t d = tmem + TM_S + 128 * (lt & 1);
+      const uint64_t b_lat = smem_desc(stage, 16, 1024, SWIZZLE_128B);
+      const uint64_t b_rope = smem_desc(stage + ROPE_OFF, 16, 512, SWIZZLE_64B);
+      const uint32_t d = tmem + TM_S + T * (lt & 1);
 #pragma unroll
       for (int ka = 0; ka < NLAT; ++ka) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f8_ss_warp(d, a_lat + ((ka * LAT_BYTES + kk * 32) >> 4), b_lat + ((ka * QLAT_BYTES + kk * 32) >> 4), ID_QK,
+          mma_f8_ts_warp(d, tmem + TM_Q + 8 * (4 * ka + kk), b_lat + ((ka * LAT_BYTES + kk * 32) >> 4), ID_QK,
                          (ka | kk) ? 1u : 0u);
       }
 #pragma unroll
@@ -584,9 +571,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     // the 4 independent d-chunks innermost: consecutive MMAs never share an accumulator
     auto issue_pv = [&](int lt) {
-      const int s = lt % NST;
+      const int s = lt % NST, pb = lt % NPB;
       const uint64_t a0 = smem_desc(kv_base + s * STAGE_BYTES, LAT_BYTES, 1024, SWIZZLE_128B);
-      const uint64_t b0 = smem_desc(p_base, P_BYTES, 512, SWIZZLE_64B);
+      const uint64_t b0 = smem_desc(p_base + pb * 2 * P_BYTES, 16, 512, SWIZZLE_64B);
 #pragma unroll
       for (int w = 0; w < 2; ++w) {
 #pragma unroll
@@ -594,34 +581,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int c = 0; c < NLAT; ++c)
             mma_f8_ss_warp(tmem + TM_O + 64 * c, a0 + ((c * LAT_BYTES + kk * 32 * 128) >> 4),
-                           b0 + ((w * P_BYTES + kk * 32 * H) >> 4), ID_PV, (lt > 0 || w > 0 || kk > 0) ? 1u : 0u);
+                           b0 + ((w * P_BYTES + kk * 32) >> 4), ID_PV, (lt > 0 || w > 0 || kk > 0) ? 1u : 0u);
         }
       }
       mma_commit_warp(bar(B_KVE + s));
-      mma_commit_warp(bar(B_PVD));
+      mma_commit_warp(bar(B_PVD + pb));
     };
-    ok = wait_warp(B_QREADY, 0) && wait_warp(B_KVF, 0);
-    if (ok) {
-      tc_fence_after_sync();
-      issue_qk(0);
+    auto kv_landed = [&](int lt) { return wait_warp(B_KVF + lt % NST, (lt / NST) & 1); };
+    if (!FUSED) convert_q((NTMA + SOFTMAX_WARPS) * 32 + lane);  // threads 480 .. 511
+    // QK^T of tiles 0 and 1 fill both S buffers
+    ok = wait_warp(B_QREADY, 0);
+    for (int lt = 0; lt < 2 && lt < ntl && ok; ++lt) {
+      ok = kv_landed(lt);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_qk(lt);
+      }
     }
     for (int lt = 0; lt < ntl && ok; ++lt) {
-      if (lt + 1 < ntl) {
-        // S buffer (lt + 1) & 1 was last read by the softmax of tile lt - 1,
-        // whose P was waited for before P V (lt - 1) was issued
-        if (!wait_warp(B_KVF + (lt + 1) % NST, ((lt + 1) / NST) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        issue_qk(lt + 1);
-      }
-      if (!wait_warp(B_PF, lt & 1)) {
+      // P(lt) written: P V(lt) goes first (the softmax of tile lt + 1 is
+      // running meanwhile); S buffer lt % 2 has been read, so QK^T(lt + 2)
+      // may overwrite it once its tile has landed
+      if (!wait_warp(B_PF + lt % NPB, (lt / NPB) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       issue_pv(lt);
+      if (lt + 2 < ntl) {
+        if (!kv_landed(lt + 2)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        issue_qk(lt + 2);
+      }
     }
     __syncwarp();
     mma_commit_warp(bar(B_OF));
@@ -631,12 +625,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp >= SOFTMAX_WARP0) {
     // ---------------- softmax warps ----------------
     const int sw = warp - SOFTMAX_WARP0;            // 0..7
-    const int q4 = warp & 3;                        // TMEM lane quadrant (warp % 4)
-    const int h2 = sw >> 2;                         // heads [32 h2, 32 h2 + 32)
-    const int hg = 2 * h2 + (lane >> 4);            // this thread's heads: [16 hg, 16 hg + 16)
-    const int j = 16 * q4 + (lane & 15);            // this thread's tile row
+    const int q4 = warp & 3;                        // TMEM lane quadrant: heads [16 q4, 16 q4 + 16)
+    const int half = sw >> 2;                       // tile rows [32 half, 32 half + 32); O heads [32 half, +32)
+    const int hh = 16 * q4 + (lane & 15);           // this thread's head
+    const int up = lane >> 4;                       // 0: this lane holds Q_hi logits, 1: Q_lo
+    const int cc = 2 * half + up;                   // after the exchange: tile rows [16 cc, 16 cc + 16)
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
-    if (!FUSED) convert_q(tid - SOFTMAX_WARP0 * 32 + NTMA * 32);
+    if (!FUSED) convert_q(tid - SOFTMAX_WARP0 * 32 + NTMA * 32);  // threads 224 .. 479
     const float qk_scale = a.softmax_scale * LOG2E * ldexpf(1.f, -*qexp_s);
     // P' = p s_j 2^E with p <= 16: pick E so that 16 max_j s_j 2^E < 256,
     // max_j over the entries of this CTA's tiles
@@ -661,110 +656,107 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     const float p_scale = ldexpf(1.f, p_exp);
+    // P' = p s_j 2^E = p c_j (2^E / qk_scale), c_j = s_j qk_scale the row's logit factor
+    const float p_ratio = p_scale / qk_scale;
 
-    float l_part[16];
-#pragma unroll
-    for (int h = 0; h < 16; ++h) l_part[h] = 0.f;
-    uint32_t ph_a = 0, ph_b = 0, ph_c = 0;  // completed phases of the group barriers
+    // head hh's reference max (log2 domain) and its share of l; the four
+    // threads of a head keep identical copies of the reference
+    float m_ref = -INFINITY, l_part = 0.f;
+    // per tile, this warp's 32 rows' logit factors, double buffered
+    float* rowf = reinterpret_cast<float*>(smem + OFF_ROWF) + sw * 2 * 32;
+    uint32_t ph_b = 0, ph_c = 0;  // completed phases of the group barriers
     auto group_sync = [&](int bb, uint32_t& ph) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(bb));
-      const bool done = wait_warp(bb, ph & 1);
+      if (ok && !wait_warp(bb, ph & 1)) ok = false;
       ++ph;
-      return done;
+      return ok;
     };
-    auto row_info = [&](int lt) -> int2 {
-      const int e = (t_begin + lt) * T + j;
+    auto row_info = [&](int lt) -> int2 {  // lane's row: 32 half + lane
+      const int e = (t_begin + lt) * T + 32 * half + lane;
       return e < a.k ? ld_res(row_res + e) : make_int2(-1, 0);
     };
     int2 info = row_info(0);
-    for (int lt = 0; lt < ntl && ok; ++lt) {
+    for (int lt = 0; lt < ntl; ++lt) {  // no early exit: every warp reaches every vote barrier
       const int sb = lt & 1;
       const int2 info_next = lt + 1 < ntl ? row_info(lt + 1) : make_int2(-1, 0);
-      if (!wait_warp(B_SF + sb, (lt >> 1) & 1)) {
-        ok = false;
-        break;
+      // the warp's rows: validity bits (bit r: row 32 half + r) and logit factors
+      const unsigned vmask = __ballot_sync(0xffffffffu, info.x >= 0);
+      rowf[sb * 32 + lane] = __int_as_float(info.y) * qk_scale;
+      __syncwarp();
+      float cj[16];  // this thread's rows' factors
+      {
+        const float4* rf4 = reinterpret_cast<const float4*>(rowf + sb * 32 + 16 * up);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 f = rf4[i];
+          cj[4 * i] = f.x;
+          cj[4 * i + 1] = f.y;
+          cj[4 * i + 2] = f.z;
+          cj[4 * i + 3] = f.w;
+        }
       }
+      if (ok && !wait_warp(B_SF + sb, (lt >> 1) & 1)) ok = false;
       tc_fence_after_sync();
-      const bool valid = info.x >= 0;
-      const float sc = __int_as_float(info.y);
-      const float cj = sc * qk_scale;
-      // logits of row j, heads 16 hg + h, in the log2 domain (invalid rows: -inf)
-      auto load_z = [&](float (&z)[16]) {
-        float vh[16], vl[16];
-        tmem_ld16x2<16>(t_lane + TM_S + 128 * sb + 32 * h2, vh);
-        tmem_ld16x2<16>(t_lane + TM_S + 128 * sb + H + 32 * h2, vl);
+      // logits of head hh, rows 16 cc + c, in the log2 domain (invalid rows: -inf):
+      // lane u holds S_hi (u < 16) or S_lo (u >= 16) of the warp's 32 rows;
+      // the partner lane u ^ 16 sends the other half of this thread's 16 rows
+      float z[16];
+      {
+        float v[32];
+        tmem_ld32(t_lane + TM_S + T * sb + 32 * half, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 16; ++h) z[h] = valid ? (vh[h] + vl[h]) * cj : -INFINITY;
-      };
-      float z[16];
-      load_z(z);
+        for (int c = 0; c < 16; ++c) {
+          const float send = up ? v[c] : v[16 + c];
+          const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+          z[c] = up ? got + v[16 + c] : v[c] + got;  // hi + lo
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) z[c] *= cj[c];
+        if (vmask != 0xffffffffu) {  // a tile with rows past the selection (warp-uniform)
+          const unsigned my_valid = vmask >> (16 * up);
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (!((my_valid >> c) & 1u)) z[c] = -INFINITY;
+        }
+      }
       // Fast path: probabilities are taken against the heads' current
       // reference maxima; that stays exact as long as no logit exceeds its
       // reference by more than 2^EXCEED.  One vote of the 8 warps decides;
       // only then is the tile maximum reduced.
       bool bad = false;
-      {
-        const float4* mu4 = reinterpret_cast<const float4*>(muse_s + 16 * hg);
 #pragma unroll
-        for (int h4 = 0; h4 < 4; ++h4) {
-          const float4 m = mu4[h4];
-          bad |= z[4 * h4] > m.x + EXCEED_LOG2;
-          bad |= z[4 * h4 + 1] > m.y + EXCEED_LOG2;
-          bad |= z[4 * h4 + 2] > m.z + EXCEED_LOG2;
-          bad |= z[4 * h4 + 3] > m.w + EXCEED_LOG2;
-        }
-        bad &= valid;
-      }
-      const unsigned bv = __ballot_sync(0xffffffffu, bad);
-      if (lane == 0) vote_s[(lt & 1) * SOFTMAX_WARPS + sw] = bv != 0u;
-      if (!group_sync(B_SYNCA, ph_a)) {
-        ok = false;
-        break;
-      }
-      int anybad = 0;
+      for (int c = 0; c < 16; ++c) bad |= z[c] > m_ref + EXCEED_LOG2;  // -inf never exceeds
+      if (named_barrier_or(3, SOFTMAX_WARPS * 32, bad)) {  // one vote of the 8 warps: uniform
+        float tm = z[0];
 #pragma unroll
-      for (int w = 0; w < SOFTMAX_WARPS; ++w) anybad |= vote_s[(lt & 1) * SOFTMAX_WARPS + w];
-      if (anybad) {  // uniform over the 8 warps
-        red_s[q4 * H + 32 * h2 + lane] = half_warp_transpose_reduce<true>(z, lane);
-        if (!group_sync(B_SYNCB, ph_b)) {
-          ok = false;
-          break;
+        for (int c = 1; c < 16; ++c) tm = fmaxf(tm, z[c]);
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+        if (up == 0) red_s[half * H + hh] = tm;
+        group_sync(B_SYNCB, ph_b);
+        const float mt = fmaxf(red_s[hh], red_s[H + hh]);
+        float alpha = 1.f;
+        if (mt > m_ref + EXCEED_LOG2) {
+          alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mt);
+          m_ref = mt;
         }
-        if (q4 == 0) {  // softmax warps 0 and 4 (quadrant 0) own 32 heads each
-          const int hh = 32 * h2 + lane;
-          const float mt = fmaxf(fmaxf(red_s[hh], red_s[H + hh]), fmaxf(red_s[2 * H + hh], red_s[3 * H + hh]));
-          const float mo = muse_s[hh];
-          float alpha = 1.f;
-          if (mt > mo + EXCEED_LOG2) {
-            alpha = (mo == -INFINITY) ? 0.f : ex2(mo - mt);
-            muse_s[hh] = mt;
-          }
-          alpha_s[hh] = alpha;
-          const unsigned need = __ballot_sync(0xffffffffu, lt > 0 && alpha != 1.f);
-          if (lane == 0) resc_s[h2] = need != 0u;
-        }
-        if (!group_sync(B_SYNCC, ph_c)) {
-          ok = false;
-          break;
-        }
-        if (resc_s[h2]) {
+        l_part *= alpha;
+        if (half == 0 && up == 0) alpha_s[hh] = alpha;
+        const unsigned need = __ballot_sync(0xffffffffu, lt > 0 && alpha != 1.f);
+        if (half == 0 && lane == 0) resc_s[q4] = need != 0u;
+        group_sync(B_SYNCC, ph_c);
+        if (resc_s[0] | resc_s[1] | resc_s[2] | resc_s[3]) {
           // O must hold every P V issued so far: the previous tile's
-          if (!wait_warp(B_PVD, (lt - 1) & 1)) {
-            ok = false;
-            break;
-          }
+          if (ok && !wait_warp(B_PVD + (lt - 1) % NPB, ((lt - 1) / NPB) & 1)) ok = false;
           tc_fence_after_sync();
-#pragma unroll
-          for (int h = 0; h < 16; ++h) l_part[h] *= alpha_s[16 * hg + h];
-          const float* al = alpha_s + 32 * h2;
+          const float* al = alpha_s + 32 * half;
 #pragma unroll 1
           for (int c = 0; c < NLAT; ++c) {
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
               float o[16];
-              const uint32_t addr = t_lane + TM_O + 64 * c + 32 * h2 + 16 * g;
+              const uint32_t addr = t_lane + TM_O + 64 * c + 32 * half + 16 * g;
               tmem_ld16(addr, o);
               tmem_wait_ld();
 #pragma unroll
@@ -774,35 +766,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           tmem_wait_st();
         }
-        load_z(z);  // S is still in TMEM: reload rather than keep z live across the rescale
       }
       // probabilities, folded with the row's dequantisation scale and the
       // query's power of two, as E4M3 hi + lo (computed before waiting for
       // the P buffer, so that only the stores wait)
+      // invalid rows have z = -inf and p = 2^-inf = 0; a head whose reference
+      // is still -inf has only such rows
       uint32_t phi[8], plo[8];
-      const float sp = sc * p_scale;
-      const float4* mu4 = reinterpret_cast<const float4*>(muse_s + 16 * hg);
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
 #pragma unroll
-      for (int h4 = 0; h4 < 4; ++h4) {
-        const float4 m = mu4[h4];
-        const float mm[4] = {m.x, m.y, m.z, m.w};
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int h = 4 * h4 + 2 * t;
-          const float p0 = valid ? ex2(z[h] - mm[2 * t]) : 0.f;
-          const float p1 = valid ? ex2(z[h + 1] - mm[2 * t + 1]) : 0.f;
-          l_part[h] += p0;
-          l_part[h + 1] += p1;
-          split_e4m3x2(f32x2_to_f16x2(p0 * sp, p1 * sp), phi[h / 2], plo[h / 2]);
-        }
+      for (int i = 0; i < 8; ++i) {
+        const float p0 = ex2(z[2 * i] - m_use), p1 = ex2(z[2 * i + 1] - m_use);
+        l_part += p0;
+        l_part += p1;
+        split_e4m3x2(f32x2_to_f16x2(p0 * (cj[2 * i] * p_ratio), p1 * (cj[2 * i + 1] * p_ratio)), phi[i], plo[i]);
       }
-      // the P buffer is free once P V of the previous tile is done
-      if (lt >= 1 && !wait_warp(B_PVD, (lt - 1) & 1)) {
-        ok = false;
-        break;
-      }
+      // P buffer lt % 2 is free once P V of tile lt - 2 is done
+      if (lt >= NPB && ok && !wait_warp(B_PVD + lt % NPB, ((lt - NPB) / NPB) & 1)) ok = false;
       {
-        unsigned char* pr = p_s + j * H + ((hg ^ ((j >> 1) & 3)) << 4);
+        unsigned char* pr = p_s + (lt % NPB) * 2 * P_BYTES + hh * T + ((cc ^ ((hh >> 1) & 3)) << 4);
         *reinterpret_cast<uint4*>(pr) = make_uint4(phi[0] | (phi[1] << 16), phi[2] | (phi[3] << 16),
                                                    phi[4] | (phi[5] << 16), phi[6] | (phi[7] << 16));
         *reinterpret_cast<uint4*>(pr + P_BYTES) = make_uint4(plo[0] | (plo[1] << 16), plo[2] | (plo[3] << 16),
@@ -811,23 +793,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PF));
+      if (lane == 0) mbar_arrive(bar(B_PF + lt % NPB));
       info = info_next;
     }
     // ---------------- epilogue: normalise and write ----------------
     if (ok && !wait_warp(B_OF, 0)) ok = false;
     if (ok) {
       tc_fence_after_sync();
-      red_s[q4 * H + 32 * h2 + lane] = half_warp_transpose_reduce<false>(l_part, lane);
+      const float lw = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);  // the warp's 32 rows
+      if (up == 0) red_s[half * H + hh] = lw;
       ok = group_sync(B_SYNCB, ph_b);
     }
     if (ok) {
-      if (q4 == 0) {
-        const int hh = 32 * h2 + lane;
-        const float l = red_s[hh] + red_s[H + hh] + red_s[2 * H + hh] + red_s[3 * H + hh];
-        const float m = muse_s[hh];
+      if (half == 0 && up == 0) {
+        const float l = red_s[hh] + red_s[H + hh];
         alpha_s[hh] = l > 0.f ? ldexpf(1.f / l, -p_exp) : 0.f;
-        const float lse = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+        const float lse = l > 0.f ? (m_ref + log2f(l)) * LN2 : -INFINITY;
         if (S == 1) {
           if (a.lse) a.lse[(int64_t)i * H + hh] = lse;
         } else {
@@ -841,6 +822,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // latent dim d = 128 c + 32 q4 + lane of its 32 heads, so a warp's
       // store covers 32 consecutive d of one head.  The 32 per-head factors
       // go to registers first.
+      const int h2 = half;
       float inv[32];
 #pragma unroll
       for (int h = 0; h < 32; ++h) inv[h] = alpha_s[32 * h2 + h];
