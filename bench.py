@@ -39,9 +39,9 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # as null once those sources change).
 TRAFFIC_BY_SOURCE: dict[str, dict] = {
     # mla_tc.cu + topk_row.cuh: the fused decode kernel (top-k + attention)
-    "79ce205c8dcb08014efef3a259bc623027d85f59": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_780_544},
+    "cbd1260e02594c4867ce51ef89538c0a60747c7c": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 85_296_128},
     # mla_tc.cu: the attention kernel as its own call
-    "d3e55d0d30aa4b887df38f62455d07029eef0a0d": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49_920_256},
+    "5cbdbfc6135f9f23b2c4579ecb663011785c3a79": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 50_270_976},
 }
 
 

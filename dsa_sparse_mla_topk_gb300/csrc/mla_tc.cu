@@ -777,8 +777,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float p0 = ex2(z[2 * i] - m_use), p1 = ex2(z[2 * i + 1] - m_use);
-        l_part += p0;
-        l_part += p1;
+        l_part += p0 + p1;
         split_e4m3x2(f32x2_to_f16x2(p0 * (cj[2 * i] * p_ratio), p1 * (cj[2 * i + 1] * p_ratio)), phi[i], plo[i]);
       }
       // P buffer lt % 2 is free once P V of tile lt - 2 is done
