@@ -113,7 +113,7 @@ constexpr int B_KVF = 0;                  // [NST] tile in stage s has landed (T
 constexpr int B_KVE = B_KVF + NST;        // [NST] stage s is free (its P V MMAs are done)
 constexpr int B_SF = B_KVE + NST;         // [2] S buffer b is complete
 constexpr int B_PF = B_SF + 2;            // [2] P buffer b is written (and O rescaled)
-constexpr int B_PVD = B_PF + NPB;         // [2] P V of the tile in P buffer b is done: b is free
+constexpr int B_PVD = B_PF + NPB;         // [2] P V of the tile in P buffer b is done (waited on before rescaling O)
 constexpr int B_OF = B_PVD + NPB;         // every P V is done
 constexpr int B_SYNCA = B_OF + 1;         // softmax-group sync points
 constexpr int B_SYNCB = B_SYNCA + 1;
@@ -780,8 +780,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         l_part += p0 + p1;
         split_e4m3x2(f32x2_to_f16x2(p0 * (cj[2 * i] * p_ratio), p1 * (cj[2 * i + 1] * p_ratio)), phi[i], plo[i]);
       }
-      // P buffer lt % 2 is free once P V of tile lt - 2 is done
-      if (lt >= NPB && ok && !wait_warp(B_PVD + lt % NPB, ((lt - NPB) / NPB) & 1)) ok = false;
+      // P buffer lt % 2 was last read by P V(lt - 2), which the MMA warp issued
+      // before QK^T(lt): the commit that completed S(lt) tracks every MMA issued
+      // before it, so the buffer is free without a wait of its own
       {
         unsigned char* pr = p_s + (lt % NPB) * 2 * P_BYTES + hh * T + ((cc ^ ((hh >> 1) & 3)) << 4);
         *reinterpret_cast<uint4*>(pr) = make_uint4(phi[0] | (phi[1] << 16), phi[2] | (phi[3] << 16),
