@@ -774,11 +774,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // is still -inf has only such rows
       uint32_t phi[8], plo[8];
       const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      // (the row factors are read again rather than kept in registers across the vote)
+      const float4* rfp = reinterpret_cast<const float4*>(rowf + sb * 32 + 16 * up);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float p0 = ex2(z[2 * i] - m_use), p1 = ex2(z[2 * i + 1] - m_use);
-        l_part += p0 + p1;
-        split_e4m3x2(f32x2_to_f16x2(p0 * (cj[2 * i] * p_ratio), p1 * (cj[2 * i + 1] * p_ratio)), phi[i], plo[i]);
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 f = rfp[k4];
+        const float cf[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int i = 2 * k4 + t;
+          const float p0 = ex2(z[2 * i] - m_use), p1 = ex2(z[2 * i + 1] - m_use);
+          l_part += p0 + p1;
+          split_e4m3x2(f32x2_to_f16x2(p0 * (cf[2 * t] * p_ratio), p1 * (cf[2 * t + 1] * p_ratio)), phi[i], plo[i]);
+        }
       }
       // P buffer lt % 2 was last read by P V(lt - 2), which the MMA warp issued
       // before QK^T(lt): the commit that completed S(lt) tracks every MMA issued
@@ -820,38 +828,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok) {
       // O^T (TMEM) -> registers -> global memory: thread (q4, lane) holds
       // latent dim d = 128 c + 32 q4 + lane of its 32 heads, so a warp's
-      // store covers 32 consecutive d of one head.  The 32 per-head factors
-      // go to registers first.
+      // store covers 32 consecutive d of one head.  The per-head factors of
+      // each group of 16 heads go to registers first.
       const int h2 = half;
-      float inv[32];
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        float inv[16];
 #pragma unroll
-      for (int h = 0; h < 32; ++h) inv[h] = alpha_s[32 * h2 + h];
-      if (S == 1) {
-        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)i * H * DL + (int64_t)(32 * h2) * DL;
+        for (int h = 0; h < 16; ++h) inv[h] = alpha_s[32 * h2 + 16 * g + h];
+        const int64_t hbase = 32 * h2 + 16 * g;
 #pragma unroll 1
         for (int c = 0; c < NLAT; ++c) {
           const int d = 128 * c + 32 * q4 + lane;
+          float o[16];
+          tmem_ld16(t_lane + TM_O + 64 * c + hbase, o);
+          tmem_wait_ld();
+          if (S == 1) {
+            __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)i * H + hbase) * DL + d;
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            float o[16];
-            tmem_ld16(t_lane + TM_O + 64 * c + 32 * h2 + 16 * g, o);
-            tmem_wait_ld();
+            for (int h = 0; h < 16; ++h) ob[h * DL] = __float2bfloat16_rn(o[h] * inv[h]);
+          } else {
+            float* op = a.o_part + (((int64_t)split * a.num_q + i) * H + hbase) * DL + d;
 #pragma unroll
-            for (int h = 0; h < 16; ++h) ob[(16 * g + h) * DL + d] = __float2bfloat16_rn(o[h] * inv[16 * g + h]);
-          }
-        }
-      } else {
-        float* op = a.o_part + ((int64_t)split * a.num_q + i) * H * DL + (int64_t)(32 * h2) * DL;
-#pragma unroll 1
-        for (int c = 0; c < NLAT; ++c) {
-          const int d = 128 * c + 32 * q4 + lane;
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            float o[16];
-            tmem_ld16(t_lane + TM_O + 64 * c + 32 * h2 + 16 * g, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 16; ++h) op[(16 * g + h) * DL + d] = o[h] * inv[16 * g + h];
+            for (int h = 0; h < 16; ++h) op[h * DL] = o[h] * inv[h];
           }
         }
       }
