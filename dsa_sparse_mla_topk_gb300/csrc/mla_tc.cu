@@ -415,15 +415,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   };
   auto convert_q = [&](int qt) { convert_q_by(qt, NTHREADS, [] { named_barrier_sync(1, NTHREADS); }, true); };
 
-  // TMA warps: warp tw's lane l copies row group tw + NTMA l (tile rows
-  // 4g .. 4g + 3) of a tile, 4 rows per copy
+  // TMA warps: a tile's 80 copies (16 row groups of 4 rows x 4 latent slices
+  // + 1 rope slice) are numbered group-major, c = 5 g + slice, and dealt out in
+  // contiguous runs of 11 or 12: lane l of TMA warp tw issues copy
+  // 80 tw / 7 + l (lanes of a warp that share a group load the same slots)
   const int tw = warp < WARP_MMA ? warp : warp - 1;
-  const int my_groups = (GROUPS - tw + NTMA - 1) / NTMA;
-  const int g = tw + NTMA * lane;
+  constexpr int NCP = (NLAT + 1) * GROUPS;  // copies per tile
+  const int cp0 = NCP * tw / NTMA, cp = cp0 + lane;
+  const bool has_cp = lane < NCP * (tw + 1) / NTMA - cp0;
+  const int g = cp / (NLAT + 1), part = cp % (NLAT + 1);
+  // this warp's bytes per tile
+  const uint32_t my_bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, has_cp && part < NLAT)) * 512u +
+                            (uint32_t)__popc(__ballot_sync(0xffffffffu, has_cp && part == NLAT)) * 256u;
   // the slots of this lane's row group of tile lt (-1: past k, read as zeros)
   auto tile_rows = [&](int lt) -> int4 {
     int r4[4] = {-1, -1, -1, -1};
-    if (g < GROUPS && lt < ntl) {
+    if (has_cp && lt < ntl) {
       const int base = (t_begin + lt) * T + 4 * g;
 #pragma unroll
       for (int q = 0; q < 4; ++q) r4[q] = base + q < a.k ? ld_res(&row_res[base + q]).x : -1;
@@ -431,14 +438,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     return make_int4(r4[0], r4[1], r4[2], r4[3]);
   };
   auto gather_tile = [&](int s, int4 rows) {  // a tile's rows into stage s (whole TMA warp)
-    if (lane == 0) mbar_arrive_expect_tx(bar(B_KVF + s), my_groups * (STAGE_BYTES / GROUPS));
+    if (lane == 0) mbar_arrive_expect_tx(bar(B_KVF + s), my_bytes);
     __syncwarp();
-    if (g < GROUPS) {
+    if (has_cp) {
       const uint32_t dst = kv_base + s * STAGE_BYTES;
-#pragma unroll
-      for (int ka = 0; ka < NLAT; ++ka)
-        tma_gather4(dst + ka * LAT_BYTES + g * 512, &tmap_lat, ka * 128, rows, bar(B_KVF + s));
-      tma_gather4(dst + ROPE_OFF + g * 256, &tmap_rope, DL, rows, bar(B_KVF + s));
+      if (part < NLAT)
+        tma_gather4(dst + part * LAT_BYTES + g * 512, &tmap_lat, part * 128, rows, bar(B_KVF + s));
+      else
+        tma_gather4(dst + ROPE_OFF + g * 256, &tmap_rope, DL, rows, bar(B_KVF + s));
     }
   };
 
