@@ -57,7 +57,10 @@ def parse_args():
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="repeat the timed block of --steps passes until about this much timed load")
     ap.add_argument("--max-blocks", type=int, default=400)
-    ap.add_argument("--no-fused", action="store_true", help="run top-k and attention as separate calls")
+    ap.add_argument("--fused", action="store_true",
+                    help="run top-k and attention in one kernel where the shape allows (slower than the default "
+                         "separate calls on every workload measured)")
+    ap.add_argument("--no-fused", action="store_true", help="separate calls (the default; kept for old commands)")
     ap.add_argument("--splits", type=int, default=0, help="KV splits (0 = library's rule)")
     ap.add_argument("--cpu-sample", type=int, default=64, help="query tokens the oracle baseline times")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -282,8 +285,8 @@ def prepare(w, dev, dsa, wl, args, torch):
     inp = wl.make_inputs(w, device=dev)
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     S = args.splits or dsa.pick_num_splits(w.num_q, w.heads, w.d_latent, w.d_rope, w.k, num_sms)
-    fused = (not args.no_fused) and dsa.use_fused_path(w.num_q, w.heads, w.d_latent, w.d_rope, inp.scores.shape[1],
-                                                        w.k, S, dev)
+    fused = args.fused and not args.no_fused and dsa.fused_path_supported(
+        w.num_q, w.heads, w.d_latent, w.d_rope, inp.scores.shape[1], w.k, S)
     bufs = {"idx": torch.empty((w.num_q, w.k), dtype=torch.int32, device=dev),
             "out": torch.empty((w.num_q, w.heads, w.d_latent), dtype=torch.bfloat16, device=dev),
             "lse": torch.empty((w.num_q, w.heads), dtype=torch.float32, device=dev)}

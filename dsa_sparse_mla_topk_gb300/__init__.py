@@ -15,7 +15,7 @@ import threading
 import torch
 
 __all__ = ["DsaError", "load_library", "topk_select", "sparse_mla_fwd", "combine", "sparse_mla_topk",
-           "sparse_mla_topk_fused", "use_fused_path", "kv_write",
+           "sparse_mla_topk_fused", "fused_path_supported", "kv_write",
            "PrefixCache",
            "kv_tile_count", "kv_tile_size", "pick_num_splits", "status_string", "EXPORTED_SYMBOLS",
            "DEV_BAD_QPOS", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT"]
@@ -345,24 +345,23 @@ def sparse_mla_topk_fused(q, kv, kv_scale, block_table, q_req, q_pos, scores, k:
     return out, lse, idx
 
 
-_SM_COUNT: dict = {}
+def fused_path_supported(num_q: int, heads: int, d_latent: int, d_rope: int, ld: int, k: int,
+                         num_splits: int) -> bool:
+    """Whether the single-kernel path (dsa_sparse_mla_topk_fwd: the row's top-k,
+    the page lookup and the Partial in one CTA per query token) can run this
+    shape: the tensor-core head shape, one KV split, rows of at most 65,536
+    positions and k within the kernel's limit.
 
-
-def use_fused_path(num_q: int, heads: int, d_latent: int, d_rope: int, ld: int, k: int, num_splits: int,
-                   device) -> bool:
-    """Whether sparse_mla_topk takes the single-kernel path: the tensor-core
-    shape, one KV split, rows of at most 65,536 positions, k within the
-    fused kernel's limit, and no more query tokens than SMs (decode).  With
-    more tokens the separate top-k kernel, which keeps two rows per SM in
-    flight, is faster."""
+    sparse_mla_topk does not pick it by itself: measured on GB300, the separate
+    calls are faster at every decode batch tried (8 to 128 requests of a 64K
+    context, and the 8-token verify and prefill shapes), because the attention
+    kernel, launched as a programmatic dependent, converts Q and sets up while
+    the top-k kernel still runs, where the single kernel does that work after
+    its own selection."""
+    del num_q
     if (heads, d_latent, d_rope) != (64, 512, 64) or num_splits != 1 or ld > 65536:
         return False
-    if k > load_library().dsa_sparse_mla_topk_max_k():
-        return False
-    dev = torch.device(device)
-    if dev not in _SM_COUNT:
-        _SM_COUNT[dev] = torch.cuda.get_device_properties(dev).multi_processor_count
-    return num_q <= _SM_COUNT[dev]
+    return k <= load_library().dsa_sparse_mla_topk_max_k()
 
 
 def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, *, d_latent: int, d_rope: int,
@@ -371,15 +370,13 @@ def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, 
     """One pass of the whole path: top-k -> Partial -> Combine (when split).
     ``buffers`` (optional) holds preallocated idx / out / lse / o_part /
     lse_part / workspace tensors.  ``fused``: True runs top-k and the Partial
-    step in one kernel (dsa_sparse_mla_topk_fwd), False as separate calls,
-    None picks by use_fused_path (the same results either way).  Returns
-    (out, lse, idx)."""
+    step in one kernel (dsa_sparse_mla_topk_fwd, where fused_path_supported),
+    False or None as separate calls, the faster path (the same results either
+    way).  Returns (out, lse, idx)."""
     b = buffers or {}
     num_q, H, _ = q.shape
     if num_splits is None:
         num_splits = pick_num_splits(num_q, H, d_latent, d_rope, k)
-    if fused is None:
-        fused = use_fused_path(num_q, H, d_latent, d_rope, scores.shape[1], k, num_splits, q.device)
     if fused:
         if num_splits != 1:
             raise ValueError("the fused path has one KV split")

@@ -525,14 +525,18 @@ def test_fused_path_equals_separate_calls(w):
     assert_close(host(o1.float())[rows], host(l1)[rows], ref_out, ref_lse, w.name + " fused")
 
 
-def test_fused_path_is_taken_for_decode_and_bad_rows_are_reported():
-    """The public pass picks the fused kernel for the decode workload, and a
-    query position outside the scores row gives BAD_QPOS, a row of -1 and an
-    empty attention (out 0, lse -inf) without faulting."""
+def test_fused_path_limits_and_bad_rows_are_reported():
+    """The single-kernel path accepts the 64-head shape with one KV split, rows
+    of up to 65,536 positions and k up to its limit; and a query position
+    outside the scores row gives BAD_QPOS, a row of -1 and an empty attention
+    (out 0, lse -inf) without faulting."""
     w = SMALL_H64
-    assert dsa.use_fused_path(128, 64, 512, 64, 65536, 2048, 1, "cuda")
-    assert not dsa.use_fused_path(1024, 64, 512, 64, 65536, 2048, 1, "cuda")
-    assert not dsa.use_fused_path(16, 64, 512, 64, 1 << 20, 2048, 1, "cuda")
+    assert dsa.fused_path_supported(128, 64, 512, 64, 65536, 2048, 1)
+    assert dsa.fused_path_supported(1024, 64, 512, 64, 65536, 2048, 1)
+    assert not dsa.fused_path_supported(16, 64, 512, 64, 1 << 20, 2048, 1)
+    assert not dsa.fused_path_supported(128, 64, 512, 64, 65536, 2048, 2)
+    assert not dsa.fused_path_supported(128, 16, 512, 64, 65536, 2048, 1)
+    assert not dsa.fused_path_supported(128, 64, 512, 64, 65536, dsa.load_library().dsa_sparse_mla_topk_max_k() + 1, 1)
     inp = inputs(w)
     qp = inp.q_pos.clone()
     qp[1] = inp.scores.shape[1] + 3
