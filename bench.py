@@ -38,10 +38,10 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # capture, keyed by the SHA-1 of the kernel sources it was taken on (reported
 # as null once those sources change).
 TRAFFIC_BY_SOURCE: dict[str, dict] = {
-    # mla_tc.cu + topk_row.cuh: the fused decode kernel (top-k + attention)
-    "cbd1260e02594c4867ce51ef89538c0a60747c7c": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 85_296_128},
+    # mla_tc.cu + topk_row.cuh: the single-kernel path (--fused: top-k + attention)
+    "c205a38c3c1a92e12a435ce9aa156381dd005704": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_571_392},
     # mla_tc.cu: the attention kernel as its own call
-    "5cbdbfc6135f9f23b2c4579ecb663011785c3a79": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 50_270_976},
+    "df7557ee984bce8576c6e78fda92460d78095a7c": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49_922_304},
 }
 
 

@@ -196,10 +196,12 @@ DSA_API dsa_status dsa_sparse_mla_fwd_noalloc(const void* q, const uint8_t* kv, 
  * with one KV split, in a single kernel: each CTA selects its own query
  * token's top k and then attends to it.  Same results, bit for bit, as the
  * two calls; [LMSYS] section 3 (the indexer's selection feeds the Partial
- * step).  Meant for decode, where there are no more query tokens than SMs:
- * the selection of one token's row no longer waits for every other row's,
- * and no kernel boundary or index round trip through memory separates the
- * two steps.  For many query tokens the separate calls are faster.
+ * step): the selection of one token's row does not wait for every other
+ * row's, and no kernel boundary separates the two steps.  Measured on GB300
+ * the two calls are nevertheless faster on every decode, verify and prefill
+ * shape tried (dsa_sparse_mla_fwd, launched after dsa_topk_select on the same
+ * stream, sets up and converts Q while the top-k still runs); this call is
+ * for callers that want one launch.
  *
  * Arguments are those of the two calls: scores, ld_scores, q_pos and k as
  * for dsa_topk_select (ld_scores at most 65,536), idx is written as that call
