@@ -42,16 +42,18 @@
 //  * TMEM holds two S buffers (2 x 64 columns), Q's latent A operand (128
 //    columns) and O^T (4 x 64 columns); shared memory holds two P buffers.
 //    QK^T runs two tiles ahead of P V: QK^T of tile t+2 is issued right after
-//    P V of tile t, while the softmax of tile t+1 runs.  All hand-offs are
-//    mbarriers; every wait is bounded in time and reports DSA_DEV_TIMEOUT
-//    instead of hanging.
+//    P V of tile t, while the softmax of tile t+1 runs.  All hand-offs
+//    between warp roles are mbarriers, and every mbarrier wait is bounded in
+//    time and reports DSA_DEV_TIMEOUT instead of hanging; the softmax warps'
+//    per-tile vote is a named barrier with an OR reduction, which every
+//    softmax warp reaches once per tile whatever happened before.
 //  * The epilogue reads O^T from TMEM and stores it, normalised, straight to
 //    global memory (bf16 output, or the fp32 partial of a KV split).
 //  * A small resolve kernel first turns every selected position into its
 //    (slot, scale) pair, fully in parallel, into caller-provided scratch;
 //    the attention kernel is its programmatic dependent and overlaps it.
-//    The fused decode variant selects its token's top k, resolves it and
-//    converts Q in its own prologue instead.
+//    The single-kernel variant (FUSED) selects its token's top k, resolves
+//    it and converts Q in its own prologue instead.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -107,7 +109,7 @@ constexpr int OFF_P = OFF_QR + QROPE_BYTES;          // [buffer][hi, lo]
 constexpr int OFF_RED = OFF_P + NPB * 2 * P_BYTES;   // [4][64] floats: reductions
 constexpr int OFF_ALPHA = OFF_RED + 4 * H * 4;       // per-head rescale factor, then 1 / l
 constexpr int OFF_ROWF = OFF_ALPHA + H * 4;          // [8 warps][2 tiles][32 rows] logit factor
-constexpr int OFF_FLAG = OFF_ROWF + SOFTMAX_WARPS * 2 * 32 * 4;  // votes [2][8], rescale flags [4], Q exponent, ...
+constexpr int OFF_FLAG = OFF_ROWF + SOFTMAX_WARPS * 2 * 32 * 4;  // rescale flags [4], Q exponent, largest scales [8]
 constexpr int OFF_BAR = OFF_FLAG + 128;
 constexpr int B_KVF = 0;                  // [NST] tile in stage s has landed (TMA transaction bytes)
 constexpr int B_KVE = B_KVF + NST;        // [NST] stage s is free (its P V MMAs are done)
@@ -115,8 +117,7 @@ constexpr int B_SF = B_KVE + NST;         // [2] S buffer b is complete
 constexpr int B_PF = B_SF + 2;            // [2] P buffer b is written (and O rescaled)
 constexpr int B_PVD = B_PF + NPB;         // [2] P V of the tile in P buffer b is done (waited on before rescaling O)
 constexpr int B_OF = B_PVD + NPB;         // every P V is done
-constexpr int B_SYNCA = B_OF + 1;         // softmax-group sync points
-constexpr int B_SYNCB = B_SYNCA + 1;
+constexpr int B_SYNCB = B_OF + 1;         // softmax-group sync points
 constexpr int B_SYNCC = B_SYNCB + 1;
 constexpr int B_FIN = B_SYNCC + 1;        // every MMA is done (teardown)
 constexpr int B_QREADY = B_FIN + 1;       // Q hi/lo is in shared memory (and the Q staging stages are free)
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __r
   }
 }
 
-// The fused decode kernel's top-k inputs (unused by the plain kernel).
+// The single-kernel path's top-k inputs (unused by the plain kernel).
 struct TopkIn {
   const float* scores;  // fp32 [num_q, ld]
   int64_t ld;
@@ -239,10 +240,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   unsigned char* p_s = smem + OFF_P;
   float* red_s = reinterpret_cast<float*>(smem + OFF_RED);
   float* alpha_s = reinterpret_cast<float*>(smem + OFF_ALPHA);
-  int* vote_s = reinterpret_cast<int*>(smem + OFF_FLAG);  // [2][8] per-tile votes (double buffered)
-  int* resc_s = vote_s + 16;                                // [4] rescale needed, per lane quadrant
-  int* qexp_s = vote_s + 20;                                // Q's power-of-two scale
-  float* smax_s = reinterpret_cast<float*>(vote_s + 21);   // [8] softmax warps' largest scales
+  int* resc_s = reinterpret_cast<int*>(smem + OFF_FLAG);  // [4] rescale needed, per lane quadrant
+  int* qexp_s = resc_s + 4;                                  // Q's power-of-two scale
+  float* smax_s = reinterpret_cast<float*>(resc_s + 5);     // [8] softmax warps' largest scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
   auto bar = [&](int b) { return smem_u32(bars + b); };
@@ -297,7 +297,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_PVD + b), 1);
     }
     mbar_init(bar(B_OF), 1);
-    mbar_init(bar(B_SYNCA), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCB), SOFTMAX_WARPS);
     mbar_init(bar(B_SYNCC), SOFTMAX_WARPS);
     mbar_init(bar(B_FIN), 1);
