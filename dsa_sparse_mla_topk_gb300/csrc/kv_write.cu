@@ -33,6 +33,30 @@ __device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
   return r;
 }
 
+// The larger of two bf16 pairs, element by element (a NaN loses to a number).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Two-wide fp32 arithmetic, each lane rounded as its scalar .rn form.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 // CH: 16-byte chunks each lane holds per row (rows of up to 32 * 8 * CH
 // values); each warp takes KVW_RPW rows, all of their loads in flight before
 // the first row is quantised (one row per warp measured fastest: more rows
@@ -76,16 +100,18 @@ __global__ void __launch_bounds__(KVW_WARPS * 32)
       continue;
     }
     const int64_t slot = (int64_t)page * page_size + p % page_size;
-    float amax = 0.f;
+    // max |x| over the lane's bf16 pairs, in bf16 (exact): the sign bits
+    // cleared, then an element-wise max
+    uint32_t m2 = 0u;
 #pragma unroll
     for (int u = 0; u < CH; ++u) {
       if (lane + 32 * u < nch) {
         const uint32_t w[4] = {v[q][u].x, v[q][u].y, v[q][u].z, v[q][u].w};
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[t] << 16)), fabsf(__uint_as_float(w[t] & 0xffff0000u))));
+        for (int t = 0; t < 4; ++t) m2 = bf16x2_max(m2, w[t] & 0x7fff7fffu);
       }
     }
+    float amax = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float scale = __fdiv_rn(amax, 448.0f);
@@ -96,13 +122,19 @@ __global__ void __launch_bounds__(KVW_WARPS * 32)
     // 2^-90 <= scale < inf this gives the IEEE quotient's E4M3 code for every
     // bf16 x with |x| <= amax (checked exhaustively against the division on
     // the GPU); other rows (tiny or non-finite maxima) divide.
+    // (Computed for a bf16 pair at a time with two-wide fp32 operations.)
     const bool fast = scale >= 0x1p-90f && scale <= 3.4028235e38f;
     const float rcp = __frcp_rn(scale);
-    auto quot = [&](float x) {
-      if (!fast) return __fdiv_rn(x, scale);
-      const float q0 = __fmul_rn(x, rcp);
-      const float qc = __fmaf_rn(__fmaf_rn(-q0, scale, x), rcp, q0);
-      return __int_as_float(__float_as_int(qc) | (__float_as_int(x) & 0x80000000));
+    const uint64_t rcp2 = f32x2(rcp, rcp), nscale2 = f32x2(-scale, -scale);
+    auto quot2 = [&](uint32_t w) -> uint32_t {  // the E4M3 codes of the pair's two quotients
+      const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xffff0000u);
+      if (!fast) return e4m3x2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));
+      const uint64_t x = f32x2(x0, x1);
+      const uint64_t q0 = mul_f32x2(x, rcp2);
+      const uint64_t qc = fma_f32x2(fma_f32x2(q0, nscale2, x), rcp2, q0);
+      const uint32_t c0 = (uint32_t)qc | (__float_as_uint(x0) & 0x80000000u);
+      const uint32_t c1 = (uint32_t)(qc >> 32) | (__float_as_uint(x1) & 0x80000000u);
+      return e4m3x2(__uint_as_float(c0), __uint_as_float(c1));
     };
     uint2* dst = reinterpret_cast<uint2*>(kv + slot * d);
 #pragma unroll
@@ -113,8 +145,7 @@ __global__ void __launch_bounds__(KVW_WARPS * 32)
         uint32_t b[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-          b[t] = scale > 0.f ? e4m3x2(quot(__uint_as_float(w[t] << 16)), quot(__uint_as_float(w[t] & 0xffff0000u)))
-                             : 0u;
+          b[t] = scale > 0.f ? quot2(w[t]) : 0u;
         dst[c] = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
       }
     }
