@@ -149,6 +149,25 @@ __device__ __forceinline__ void split_e4m3x2(uint32_t h2, uint32_t& hi, uint32_t
   hi = a;
   lo = b;
 }
+// Two-wide fp32 arithmetic, each lane rounded as its scalar .rn form.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float x0, float x1) {
   const __half2 h = __floats2half2_rn(x0, x1);  // x0 in the low half
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -712,14 +731,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float v[32];
         tmem_ld32(t_lane + TM_S + T * sb + 32 * half, v);
         tmem_wait_ld();
+        float got[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float send = up ? v[c] : v[16 + c];
-          const float got = __shfl_xor_sync(0xffffffffu, send, 16);
-          z[c] = up ? got + v[16 + c] : v[c] + got;  // hi + lo
+        for (int c = 0; c < 16; ++c) got[c] = __shfl_xor_sync(0xffffffffu, up ? v[c] : v[16 + c], 16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // (hi + lo) c_j, two rows at a time
+          const uint64_t mine = up ? pk2(v[16 + 2 * i], v[17 + 2 * i]) : pk2(v[2 * i], v[2 * i + 1]);
+          upk2(mul2(add2(mine, pk2(got[2 * i], got[2 * i + 1])), pk2(cj[2 * i], cj[2 * i + 1])), z[2 * i], z[2 * i + 1]);
         }
-#pragma unroll
-        for (int c = 0; c < 16; ++c) z[c] *= cj[c];
         if (vmask != 0xffffffffu) {  // a tile with rows past the selection (warp-uniform)
           const unsigned my_valid = vmask >> (16 * up);
 #pragma unroll
@@ -780,6 +799,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // is still -inf has only such rows
       uint32_t phi[8], plo[8];
       const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      const uint64_t nm2 = pk2(-m_use, -m_use), ratio2 = pk2(p_ratio, p_ratio);
       // (the row factors are read again rather than kept in registers across the vote)
       const float4* rfp = reinterpret_cast<const float4*>(rowf + sb * 32 + 16 * up);
 #pragma unroll
@@ -789,9 +809,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int i = 2 * k4 + t;
-          const float p0 = ex2(z[2 * i] - m_use), p1 = ex2(z[2 * i + 1] - m_use);
+          float d0, d1;
+          upk2(add2(pk2(z[2 * i], z[2 * i + 1]), nm2), d0, d1);
+          const float p0 = ex2(d0), p1 = ex2(d1);
           l_part += p0 + p1;
-          split_e4m3x2(f32x2_to_f16x2(p0 * (cf[2 * t] * p_ratio), p1 * (cf[2 * t + 1] * p_ratio)), phi[i], plo[i]);
+          float q0, q1;
+          upk2(mul2(pk2(p0, p1), mul2(pk2(cf[2 * t], cf[2 * t + 1]), ratio2)), q0, q1);
+          split_e4m3x2(f32x2_to_f16x2(q0, q1), phi[i], plo[i]);
         }
       }
       // P buffer lt % 2 was last read by P V(lt - 2), which the MMA warp issued
