@@ -39,9 +39,9 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # as null once those sources change).
 TRAFFIC_BY_SOURCE: dict[str, dict] = {
     # mla_tc.cu + topk_row.cuh: the single-kernel path (--fused: top-k + attention)
-    "c205a38c3c1a92e12a435ce9aa156381dd005704": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_571_392},
+    "0503fd07a80830647362b06d12943cf45dc9fdd5": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_528_128},
     # mla_tc.cu: the attention kernel as its own call
-    "df7557ee984bce8576c6e78fda92460d78095a7c": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 49_922_304},
+    "34f2ea79ef5bcd5f847df0dd6062f1aa99d4e247": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 50_098_176},
 }
 
 
