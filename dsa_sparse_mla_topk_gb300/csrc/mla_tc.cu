@@ -382,7 +382,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) split_e4m3x2(f32x2_to_f16x2(bf_lo(w[t]) * qs, bf_hi(w[t]) * qs), hi[t], lo[t]);
+      for (int t = 0; t < 4; ++t) {
+        float y0, y1;
+        upk2(mul2(pk2(bf_lo(w[t]), bf_hi(w[t])), pk2(qs, qs)), y0, y1);
+        split_e4m3x2(f32x2_to_f16x2(y0, y1), hi[t], lo[t]);
+      }
       hv = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
       lv = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
     };
@@ -750,13 +754,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // reference maxima; that stays exact as long as no logit exceeds its
       // reference by more than 2^EXCEED.  One vote of the 8 warps decides;
       // only then is the tile maximum reduced.
-      bool bad = false;
+      float tm = z[0];  // this thread's largest logit (-inf when none is valid)
 #pragma unroll
-      for (int c = 0; c < 16; ++c) bad |= z[c] > m_ref + EXCEED_LOG2;  // -inf never exceeds
-      if (named_barrier_or(3, SOFTMAX_WARPS * 32, bad)) {  // one vote of the 8 warps: uniform
-        float tm = z[0];
-#pragma unroll
-        for (int c = 1; c < 16; ++c) tm = fmaxf(tm, z[c]);
+      for (int c = 1; c < 16; ++c) tm = fmaxf(tm, z[c]);
+      if (named_barrier_or(3, SOFTMAX_WARPS * 32, tm > m_ref + EXCEED_LOG2)) {  // one vote of the 8 warps: uniform
         tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
         if (up == 0) red_s[half * H + hh] = tm;
         group_sync(B_SYNCB, ph_b);
@@ -876,7 +877,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (S == 1) {
             __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)i * H + hbase) * DL + d;
 #pragma unroll
-            for (int h = 0; h < 16; ++h) ob[h * DL] = __float2bfloat16_rn(o[h] * inv[h]);
+            for (int h = 0; h < 16; h += 2) {
+              float y0, y1;
+              upk2(mul2(pk2(o[h], o[h + 1]), pk2(inv[h], inv[h + 1])), y0, y1);
+              ob[h * DL] = __float2bfloat16_rn(y0);
+              ob[(h + 1) * DL] = __float2bfloat16_rn(y1);
+            }
           } else {
             float* op = a.o_part + (((int64_t)split * a.num_q + i) * H + hbase) * DL + d;
 #pragma unroll
