@@ -690,7 +690,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // head hh's reference max (log2 domain) and its share of l; the four
     // threads of a head keep identical copies of the reference
-    float m_ref = -INFINITY, l_part = 0.f;
+    float m_ref = -INFINITY;
+    uint64_t l2 = pk2(0.f, 0.f);  // head hh's share of l, two running sums
     // per tile, this warp's 32 rows' logit factors, double buffered
     float* rowf = reinterpret_cast<float*>(smem + OFF_ROWF) + sw * 2 * 32;
     uint32_t ph_b = 0, ph_c = 0;  // completed phases of the group barriers
@@ -767,7 +768,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mt);
           m_ref = mt;
         }
-        l_part *= alpha;
+        l2 = mul2(l2, pk2(alpha, alpha));
         if (half == 0 && up == 0) alpha_s[hh] = alpha;
         const unsigned need = __ballot_sync(0xffffffffu, lt > 0 && alpha != 1.f);
         if (half == 0 && lane == 0) resc_s[q4] = need != 0u;
@@ -813,7 +814,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           float d0, d1;
           upk2(add2(pk2(z[2 * i], z[2 * i + 1]), nm2), d0, d1);
           const float p0 = ex2(d0), p1 = ex2(d1);
-          l_part += p0 + p1;
+          l2 = add2(l2, pk2(p0, p1));
           float q0, q1;
           upk2(mul2(pk2(p0, p1), mul2(pk2(cf[2 * t], cf[2 * t + 1]), ratio2)), q0, q1);
           split_e4m3x2(f32x2_to_f16x2(q0, q1), phi[i], plo[i]);
@@ -839,6 +840,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && !wait_warp(B_OF, 0)) ok = false;
     if (ok) {
       tc_fence_after_sync();
+      float la, lb;
+      upk2(l2, la, lb);
+      const float l_part = la + lb;
       const float lw = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);  // the warp's 32 rows
       if (up == 0) red_s[half * H + hh] = lw;
       ok = group_sync(B_SYNCB, ph_b);
