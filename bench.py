@@ -39,9 +39,9 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # as null once those sources change).
 TRAFFIC_BY_SOURCE: dict[str, dict] = {
     # mla_tc.cu + topk_row.cuh: the single-kernel path (--fused: top-k + attention)
-    "0503fd07a80830647362b06d12943cf45dc9fdd5": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_528_128},
+    "ee7a9972fada1028b6cbf25b06839e72ae9694b9": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_270_848},
     # mla_tc.cu: the attention kernel as its own call
-    "34f2ea79ef5bcd5f847df0dd6062f1aa99d4e247": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 50_098_176},
+    "8b211b7e389af95af75d1d27250dd61da8578bf5": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 50_037_248},
 }
 
 
