@@ -296,10 +296,17 @@ __global__ void __launch_bounds__(RNT, 2)
       vis = (int)(p + 1);  // <= ld <= RMAXV
     }
   }
-  // output slot o gets the element at offset q of s
+  // output slot o gets the element at offset q of s.  With k <= RLCAP the
+  // slice and merge kernels keep q in shared memory (where the candidate keys
+  // were, read by then) and look the outputs up afterwards, all of a thread's
+  // loads at once, instead of one dependent load per output.
+  int32_t* chosen = reinterpret_cast<int32_t*>(ckey);
+  const bool deferred = MODE != ROW_PLAIN && k <= RLCAP;
   auto emit = [&](uint32_t o, int32_t q) {
     if (MODE == ROW_PLAIN) {
       out[o] = q;
+    } else if (deferred) {
+      chosen[o] = q;
     } else if (MODE == ROW_SLICE) {
       ws_pos[wbase + o] = (int32_t)(first + q);
       ws_score[wbase + o] = s[q];
@@ -308,6 +315,18 @@ __global__ void __launch_bounds__(RNT, 2)
     }
   };
   row_select(s, vis, k, emit, ckey, hist, above_bm, equal_bm, cpos, warp_buf, sel, minmax, wcount);
+  if (deferred) {
+    __syncthreads();
+    if (MODE == ROW_SLICE) {
+      for (int j = tid; j < k; j += RNT) {
+        const int32_t q = chosen[j];
+        ws_pos[wbase + j] = (int32_t)(first + q);
+        ws_score[wbase + j] = s[q];
+      }
+    } else {
+      for (int j = tid; j < k; j += RNT) out[j] = ws_pos[wbase + chosen[j]];
+    }
+  }
 }
 
 template <int C>

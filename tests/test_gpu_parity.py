@@ -474,14 +474,16 @@ def test_topk_edges_bit_exact(ld):
 
 def test_topk_long_rows_paths_and_large_k():
     """Rows longer than 65,536 positions: the sliced path with slices shorter
-    than k, empty slices and a bad q_pos row; and k so large that the union of
+    than k, empty slices and a bad q_pos row (k = 9000 is above the 8,192
+    outputs whose lookups the slice and merge kernels defer to one pass at
+    the end, so it takes their direct path); and k so large that the union of
     the slices' blocks exceeds a row, which takes the in-place path by itself."""
     g = torch.Generator().manual_seed(53)
     ld = 200003
     sc = torch.randn((6, ld), generator=g)
     sc[2, 131072:] += 3.0                       # the last slices hold the large scores
     q_pos = np.array([ld - 1, 65536, 131071, 70000, 200000, ld + 5], dtype=np.int32)
-    for k in (100, 2048, 20000):
+    for k in (100, 2048, 9000, 20000):
         qp = q_pos.copy()
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         idx = dsa.topk_select(sc.cuda(), torch.from_numpy(qp).cuda(), k, dev_status=status)
