@@ -354,10 +354,9 @@ def fused_path_supported(num_q: int, heads: int, d_latent: int, d_rope: int, ld:
 
     sparse_mla_topk does not pick it by itself: measured on GB300, the separate
     calls are faster at every decode batch tried (8 to 128 requests of a 64K
-    context, and the 8-token verify and prefill shapes), because the attention
-    kernel, launched as a programmatic dependent, converts Q and sets up while
-    the top-k kernel still runs, where the single kernel does that work after
-    its own selection."""
+    context, and the 8-token verify and prefill shapes): the single kernel's
+    selection and tile loop run a little slower, and it cannot split the KV
+    range, which the small batches need."""
     del num_q
     if (heads, d_latent, d_rope) != (64, 512, 64) or num_splits != 1 or ld > 65536:
         return False

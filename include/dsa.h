@@ -199,8 +199,8 @@ DSA_API dsa_status dsa_sparse_mla_fwd_noalloc(const void* q, const uint8_t* kv, 
  * step): the selection of one token's row does not wait for every other
  * row's, and no kernel boundary separates the two steps.  Measured on GB300
  * the two calls are nevertheless faster on every decode, verify and prefill
- * shape tried (dsa_sparse_mla_fwd, launched after dsa_topk_select on the same
- * stream, sets up and converts Q while the top-k still runs); this call is
+ * shape tried: this kernel's selection and tile loop run a little slower,
+ * and it cannot split the KV range, which small batches need; this call is
  * for callers that want one launch.
  *
  * Arguments are those of the two calls: scores, ld_scores, q_pos and k as
