@@ -181,44 +181,67 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float x0, float x1) {
 // (normally the top-k, whose indices it reads), and the attention kernel is
 // its programmatic dependent: that starts (Q copy and split) while this runs
 // and waits for it before reading `res`.
-__global__ void __launch_bounds__(256) resolve_kernel(const MlaArgs a, int2* __restrict__ res) {
+constexpr int RES_THREADS = 256;
+// RES_ENT entries per thread: block (x, y) resolves entries
+// [256 RES_ENT x, 256 RES_ENT (x + 1)) of query y, thread t the entries
+// 256 RES_ENT x + 256 e + t.  Each of the chain's three dependent loads
+// (index, block table, scale) is issued for all of a thread's entries before
+// the next, so a thread waits for three round trips whatever RES_ENT is.  One
+// entry per thread while the call fits in about two waves of threads (the
+// most CTAs for the latency chain); eight beyond that, so that a large call
+// (verify, prefill) takes about one wave instead of many.
+template <int RES_ENT>
+__global__ void __launch_bounds__(RES_THREADS) resolve_kernel(const MlaArgs a, int2* __restrict__ res) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // block (x, y): entries [256 x, 256 x + 256) of query y
   const int64_t i = blockIdx.y;
-  const int j = blockIdx.x * 256 + threadIdx.x;
+  const int j0 = blockIdx.x * RES_THREADS * RES_ENT + threadIdx.x;
   // block 0 of each query also pulls the query's Q (72 KB) into L2 for the
   // attention kernel's bulk copy
   if (blockIdx.x == 0) {
     const char* qb = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(a.q) + i * H * DQK);
-    for (int off = threadIdx.x * 128; off < H * DQK * 2; off += 256 * 128)
+    for (int off = threadIdx.x * 128; off < H * DQK * 2; off += RES_THREADS * 128)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + off));
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the indices are complete
-  if (j < a.k) {
-    const int64_t e = i * a.k + j;
-    const int32_t pos = a.idx[e];
-    int32_t slot = -1;
-    float sc = 0.f;
-    if (pos < -1) {
+  const int32_t r = a.q_req[i];
+  const bool req_ok = r >= 0 && r < a.num_req;
+  int32_t pos[RES_ENT], page[RES_ENT];
+#pragma unroll
+  for (int e = 0; e < RES_ENT; ++e) {
+    const int j = j0 + RES_THREADS * e;
+    pos[e] = j < a.k ? a.idx[i * a.k + j] : -1;
+  }
+#pragma unroll
+  for (int e = 0; e < RES_ENT; ++e) {
+    page[e] = -1;
+    if (pos[e] >= 0 && req_ok && pos[e] / a.page_size < a.bt_stride)
+      page[e] = a.block_table[(int64_t)r * a.bt_stride + pos[e] / a.page_size];
+  }
+  int32_t slot[RES_ENT];
+  float sc[RES_ENT];
+#pragma unroll
+  for (int e = 0; e < RES_ENT; ++e) {
+    slot[e] = -1;
+    sc[e] = 0.f;
+    if (pos[e] < -1) {
       report(a.dev_status, DSA_DEV_BAD_INDEX);
-    } else if (pos >= 0) {
-      const int32_t r = a.q_req[i];
-      const int32_t pg = pos / a.page_size;
-      if (r < 0 || r >= a.num_req) {
+    } else if (pos[e] >= 0) {
+      if (!req_ok) {
         report(a.dev_status, DSA_DEV_BAD_PAGE);
-      } else if (pg >= a.bt_stride) {
+      } else if (pos[e] / a.page_size >= a.bt_stride) {
         report(a.dev_status, DSA_DEV_BAD_INDEX);
+      } else if (page[e] < 0 || page[e] >= a.num_pages) {
+        report(a.dev_status, DSA_DEV_BAD_PAGE);
       } else {
-        const int32_t page = a.block_table[(int64_t)r * a.bt_stride + pg];
-        if (page < 0 || page >= a.num_pages) {
-          report(a.dev_status, DSA_DEV_BAD_PAGE);
-        } else {
-          slot = page * a.page_size + pos % a.page_size;
-          sc = a.kv_scale[slot];
-        }
+        slot[e] = page[e] * a.page_size + pos[e] % a.page_size;
+        sc[e] = a.kv_scale[slot[e]];
       }
     }
-    res[e] = make_int2(slot, __float_as_int(sc));
+  }
+#pragma unroll
+  for (int e = 0; e < RES_ENT; ++e) {
+    const int j = j0 + RES_THREADS * e;
+    if (j < a.k) res[i * a.k + j] = make_int2(slot[e], __float_as_int(sc[e]));
   }
 }
 
@@ -958,12 +981,16 @@ cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t rcfg = {};
-  rcfg.gridDim = dim3((a.k + 255) / 256, a.num_q);
-  rcfg.blockDim = dim3(256);
+  // one entry per thread up to two waves of 2,048 threads per SM, else eight
+  const bool wide = (int64_t)a.num_q * a.k > (int64_t)device_sm_count() * 2048 * 2;
+  const int ent = wide ? 8 : 1;
+  rcfg.gridDim = dim3((a.k + RES_THREADS * ent - 1) / (RES_THREADS * ent), a.num_q);
+  rcfg.blockDim = dim3(RES_THREADS);
   rcfg.stream = stream;
   rcfg.attrs = attr;
   rcfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&rcfg, resolve_kernel, a, res);
+  cudaError_t e = wide ? cudaLaunchKernelEx(&rcfg, resolve_kernel<8>, a, res)
+                       : cudaLaunchKernelEx(&rcfg, resolve_kernel<1>, a, res);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;

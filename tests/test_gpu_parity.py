@@ -232,6 +232,56 @@ def test_bad_inputs_set_status_without_faulting():
     assert torch.isfinite(out.float()).all()
 
 
+# 320 query tokens x 2048 entries: past two waves of one-entry threads, so the
+# resolve step runs its eight-entries-per-thread variant (SMALL_H64 runs the
+# one-entry variant)
+RESOLVE_WIDE = wl.Workload("resolve_wide_320q", 40, 8, 64, 512, 64, 3000, 0, 64, 2048, seed=23)
+
+
+@pytest.mark.parametrize("w", [SMALL_H64, RESOLVE_WIDE], ids=lambda w: w.name)
+def test_resolve_reports_bad_entries_and_drops_them(w):
+    """Bad entries on the tensor-core path: each is reported in dev_status and
+    attended as if it were padding (-1), bit for bit, whichever of a thread's
+    entries it is."""
+    inp = inputs(w)
+    kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+    idx = dsa.topk_select(inp.scores, inp.q_pos, w.k)
+
+    def attend(ix, bt=None, q_req=None, st=None):
+        return dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table if bt is None else bt,
+                                  inp.q_req if q_req is None else q_req, ix, dev_status=st, **kw)
+
+    def check(flag, ref_idx, **bad):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out, lse = attend(st=st, **bad)
+        out_ref, lse_ref = attend(ref_idx)
+        torch.cuda.synchronize()
+        assert int(st.item()) & flag
+        assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
+
+    last = w.num_q - 1
+    # an index below -1 (first entry), a position past the block table (last entry of a row)
+    for (r, c), v in (((0, 0), -7), ((1, w.k - 1), 10 ** 6), ((last, 1100), -2)):
+        bad, ref = idx.clone(), idx.clone()
+        bad[r, c], ref[r, c] = v, -1
+        check(dsa.DEV_BAD_INDEX, ref, ix=bad)
+    # a page id out of range: every entry on that page of that request
+    bt = inp.block_table.clone()
+    bt[0, 1] = 10 ** 6
+    ref = idx.clone()
+    rows = (inp.q_req == 0).nonzero().flatten()
+    sub = ref[rows]
+    sub[(sub >= 0) & (sub // w.page_size == 1)] = -1
+    ref[rows] = sub
+    check(dsa.DEV_BAD_PAGE, ref, ix=idx, bt=bt)
+    # a query token whose request id is out of range: its whole row
+    q_req = inp.q_req.clone()
+    q_req[last] = w.num_req + 3
+    ref = idx.clone()
+    ref[last] = -1
+    check(dsa.DEV_BAD_PAGE, ref, ix=idx, q_req=q_req)
+
+
 def test_empty_selection_gives_zero_and_minus_inf():
     w = SMALL_H64
     inp = inputs(w)
