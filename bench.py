@@ -256,7 +256,7 @@ def bench_reference(args):
         return 0
     import oracle
     oracle.build()
-    w = wl.WORKLOADS[args.workload]
+    w = wl.lookup(args.workload)
     inp = wl.make_inputs(w, device="cpu")
     import torch
     host = host_copies(inp)
@@ -492,7 +492,7 @@ def bench_ours(args):
         sampler.__enter__()
     wall0 = time.perf_counter()
     for n in names:
-        c = prepare(wl.WORKLOADS[n], dev, dsa, wl, args, torch)
+        c = prepare(wl.lookup(n), dev, dsa, wl, args, torch)
         reports[n] = measure(dsa, c, args, torch, dev, stream, status, flush, world, barrier, peaks)
         if head is None:
             head = c

@@ -77,6 +77,17 @@ PREFILL_32K = Workload("prefill_32k_on_32k", 1, 32768, 64, 512, 64, 65536, 0, 64
 CTX_1M = Workload("ctx_1m_4x4", 4, 4, 64, 512, 64, 1 << 20, 0, 64, 2048, seed=4, spike_frac=0.001)
 WORKLOADS = {w.name: w for w in (TINY, DECODE_64K, VERIFY_64K, PREFILL_32K, CTX_1M)}
 
+# Smaller cases of the same kernels for profiler captures (a few hundred MB on
+# the device): the verify block with 19 requests, 152 query tokens, one
+# attention CTA per SM, its pool (717 MB) still far larger than L2.
+VERIFY_64K_ONE_WAVE = replace(VERIFY_64K, name="verify_64k_8tok_19req", num_req=19)
+PROFILE_CASES = {w.name: w for w in (VERIFY_64K_ONE_WAVE,)}
+
+
+def lookup(name: str) -> Workload:
+    """A measured workload, else a profiling case, by name."""
+    return WORKLOADS[name] if name in WORKLOADS else PROFILE_CASES[name]
+
 
 def shrink(w: Workload, **kw) -> Workload:
     return replace(w, **kw)
