@@ -37,11 +37,11 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
 # capture, keyed by the SHA-1 of the kernel sources it was taken on (reported
 # as null once those sources change).
-TRAFFIC_BY_SOURCE: dict[str, dict] = {
+TRAFFIC_BY_SOURCE: dict[str, dict[str, int]] = {
     # mla_tc.cu + topk_row.cuh: the single-kernel path (--fused: top-k + attention)
-    "ee7a9972fada1028b6cbf25b06839e72ae9694b9": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 84_270_848},
+    "d9b9a8f574569d7f9bd71d1e9fa3b406a43d6215": {"decode_64k_prefix99.9": 84_538_624},
     # mla_tc.cu: the attention kernel as its own call
-    "8b211b7e389af95af75d1d27250dd61da8578bf5": {"workload": "decode_64k_prefix99.9", "bytes_per_launch": 50_037_248},
+    "5817996d9822e52bf7eae1fddb14e1758bf1e3e2": {"decode_64k_prefix99.9": 49_836_032},
 }
 
 
@@ -302,17 +302,23 @@ def prepare(w, dev, dsa, wl, args, torch):
     flops, bytes_fwd, bytes_topk = algorithmic(w, inp.q_pos.cpu().numpy())
     kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
     # kernels of this library launched by one pass
+    two = not fused and dsa.two_kernel_path_supported(w.heads, w.d_latent, w.d_rope, inp.scores.shape[1])
     if fused:
-        launches = 1
+        launches, path = 1, "fused"
+    elif two:
+        launches, path = 2 + (1 if S > 1 else 0), "two kernels (top-k with the page lookup, attention)"
     else:
-        launches = (2 if topk_ws else 1) + (2 if ws_bytes else 1) + (1 if S > 1 else 0)
+        launches, path = (2 if topk_ws else 1) + (2 if ws_bytes else 1) + (1 if S > 1 else 0), "separate calls"
     return {"w": w, "inp": inp, "S": S, "fused": fused, "bufs": bufs, "kw": kw, "flops": flops,
-            "bytes_fwd": bytes_fwd, "bytes_topk": bytes_topk, "launches": launches, "ws_bytes": ws_bytes}
+            "bytes_fwd": bytes_fwd, "bytes_topk": bytes_topk, "launches": launches, "ws_bytes": ws_bytes,
+            "path": path}
 
 
 def one_pass(dsa, c, stream, status):
     """One pass of the whole path through the public call (top-k -> Partial
-    -> Combine when split; top-k and Partial in one kernel on the fused path)."""
+    -> Combine when split: on the tensor-core shape the top-k with the page
+    lookup, then the attention kernel; top-k and Partial in one kernel on the
+    fused path)."""
     w, inp = c["w"], c["inp"]
     dsa.sparse_mla_topk(inp.q, inp.kv, inp.kv_scale, inp.block_table, inp.q_req, inp.q_pos, inp.scores, w.k,
                         num_splits=c["S"], buffers=c["bufs"], dev_status=status, stream=stream, fused=c["fused"],
@@ -422,8 +428,7 @@ def measure(dsa, c, args, torch, dev, stream, status, flush, world, barrier, pea
     src_files = ["mla_tc.cu", "topk_row.cuh"] if c["fused"] else ["mla_tc.cu"]
     sha = hashlib.sha1(b"".join(open(os.path.join(ROOT, "dsa_sparse_mla_topk_gb300", "csrc", f), "rb").read()
                                 for f in src_files)).hexdigest()
-    tr = TRAFFIC_BY_SOURCE.get(sha)
-    traffic = tr["bytes_per_launch"] if tr and tr.get("workload") == w.name else None
+    traffic = TRAFFIC_BY_SOURCE.get(sha, {}).get(w.name)
     if c["fused"]:
         # the one kernel is the whole pass: its algorithmic bytes are the pass's
         kern, kbytes, kms = "sparse_mla_topk_fwd (top-k + attention, one kernel)", bytes_path, ms_per_step
@@ -436,7 +441,7 @@ def measure(dsa, c, args, torch, dev, stream, status, flush, world, barrier, pea
         "ms_per_step": ms_per_step,
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms),
                     "count": len(step_ms)},
-        "path": "fused" if c["fused"] else "separate calls", "kv_splits": c["S"],
+        "path": c["path"], "kv_splits": c["S"],
         "gpu_launches_per_step": c["launches"],
         "roofline": {"kernel": kern, "bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,

@@ -15,7 +15,8 @@ import threading
 import torch
 
 __all__ = ["DsaError", "load_library", "topk_select", "sparse_mla_fwd", "combine", "sparse_mla_topk",
-           "sparse_mla_topk_fused", "fused_path_supported", "kv_write",
+           "topk_sparse_mla_fwd", "two_kernel_path_supported", "sparse_mla_topk_fused", "fused_path_supported",
+           "kv_write",
            "PrefixCache",
            "kv_tile_count", "kv_tile_size", "pick_num_splits", "status_string", "EXPORTED_SYMBOLS",
            "DEV_BAD_QPOS", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT"]
@@ -28,7 +29,7 @@ DEV_BAD_QPOS, DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/dsa.h declares.
 EXPORTED_SYMBOLS = ("dsa_status_string", "dsa_version", "dsa_topk_select", "dsa_topk_workspace_size",
                     "dsa_sparse_mla_fwd", "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_fwd_noalloc",
-                    "dsa_sparse_mla_topk_fwd", "dsa_sparse_mla_topk_max_k",
+                    "dsa_sparse_mla_topk_fwd", "dsa_sparse_mla_topk_max_k", "dsa_topk_sparse_mla_fwd",
                     "dsa_combine", "dsa_kv_write", "dsa_prefix_cache_create", "dsa_prefix_cache_destroy",
                     "dsa_prefix_cache_acquire", "dsa_prefix_cache_release", "dsa_prefix_cache_stats",
                     "dsa_kv_tile_count", "dsa_kv_tile_size", "dsa_pick_num_splits")
@@ -72,6 +73,9 @@ def load_library(path: str | None = None):
         lib.dsa_sparse_mla_topk_fwd.argtypes = [vp, i64, vp, i32, vp, vp, vp, vp, i64, vp, i32, i32, vp, i32, i32, i32,
                                                 i32, i32, f32, vp, vp, vp, sz, vp, vp]
         lib.dsa_sparse_mla_topk_fwd.restype = i32
+        lib.dsa_topk_sparse_mla_fwd.argtypes = [vp, i64, vp, i32, vp, vp, vp, vp, i64, vp, i32, i32, vp, i32, i32,
+                                                i32, i32, i32, f32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+        lib.dsa_topk_sparse_mla_fwd.restype = i32
         lib.dsa_sparse_mla_topk_max_k.argtypes = []
         lib.dsa_sparse_mla_topk_max_k.restype = i32
         lib.dsa_sparse_mla_workspace_size.argtypes = [i32, i32, i32, i32, i32]
@@ -345,6 +349,51 @@ def sparse_mla_topk_fused(q, kv, kv_scale, block_table, q_req, q_pos, scores, k:
     return out, lse, idx
 
 
+def two_kernel_path_supported(heads: int, d_latent: int, d_rope: int, ld: int) -> bool:
+    """Whether topk_sparse_mla_fwd takes this shape: the tensor-core head
+    shape and rows of at most 65,536 positions (any k, any KV split)."""
+    return (heads, d_latent, d_rope) == (64, 512, 64) and ld <= 65536
+
+
+def topk_sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, *, d_latent: int, d_rope: int,
+                        page_size: int, softmax_scale: float, num_splits: int = 1, idx=None, out=None, lse=None,
+                        o_part=None, lse_part=None, workspace=None, dev_status=None, stream=None):
+    """topk_select followed by sparse_mla_fwd as two kernels, the top-k also
+    looking up each selected position's page and scale
+    (dsa_topk_sparse_mla_fwd); bit for bit the results of the two calls.
+    Returns (out, lse, idx), or (o_part, lse_part, idx) when num_splits > 1."""
+    for t, name, dt in ((q, "q", torch.bfloat16), (kv, "kv", torch.uint8), (kv_scale, "kv_scale", torch.float32),
+                        (block_table, "block_table", torch.int32), (q_req, "q_req", torch.int32),
+                        (q_pos, "q_pos", torch.int32), (scores, "scores", torch.float32)):
+        _check(t, name, dt)
+    num_q, H, dqk = q.shape
+    if dqk != d_latent + d_rope or kv.shape[1] != dqk or kv.shape[0] % page_size:
+        raise ValueError("q / kv row sizes do not match d_latent + d_rope, or kv is not whole pages")
+    dev = q.device
+    if idx is None:
+        idx = torch.empty((num_q, k), dtype=torch.int32, device=dev)
+    if num_splits == 1:
+        if out is None:
+            out = torch.empty((num_q, H, d_latent), dtype=torch.bfloat16, device=dev)
+        if lse is None:
+            lse = torch.empty((num_q, H), dtype=torch.float32, device=dev)
+    else:
+        if o_part is None:
+            o_part = torch.empty((num_splits, num_q, H, d_latent), dtype=torch.float32, device=dev)
+        if lse_part is None:
+            lse_part = torch.empty((num_splits, num_q, H), dtype=torch.float32, device=dev)
+    ws_bytes = sparse_mla_workspace_size(num_q, H, d_latent, d_rope, k)
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _call("dsa_topk_sparse_mla_fwd", _p(scores), scores.shape[1], _p(q_pos), k, _p(idx), _p(q), _p(kv),
+          _p(kv_scale), kv.shape[0] // page_size, _p(block_table), block_table.shape[0], block_table.shape[1],
+          _p(q_req), num_q, H, d_latent, d_rope, page_size, float(softmax_scale), num_splits,
+          _p(out) if num_splits == 1 else None, _p(lse) if num_splits == 1 else None,
+          _p(o_part) if num_splits > 1 else None, _p(lse_part) if num_splits > 1 else None,
+          _p(workspace) if ws_bytes else None, ws_bytes, _p(dev_status), _stream(stream))
+    return (out, lse, idx) if num_splits == 1 else (o_part, lse_part, idx)
+
+
 def fused_path_supported(num_q: int, heads: int, d_latent: int, d_rope: int, ld: int, k: int,
                          num_splits: int) -> bool:
     """Whether the single-kernel path (dsa_sparse_mla_topk_fwd: the row's top-k,
@@ -369,9 +418,11 @@ def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, 
     """One pass of the whole path: top-k -> Partial -> Combine (when split).
     ``buffers`` (optional) holds preallocated idx / out / lse / o_part /
     lse_part / workspace tensors.  ``fused``: True runs top-k and the Partial
-    step in one kernel (dsa_sparse_mla_topk_fwd, where fused_path_supported),
-    False or None as separate calls, the faster path (the same results either
-    way).  Returns (out, lse, idx)."""
+    step in one kernel (dsa_sparse_mla_topk_fwd, where fused_path_supported);
+    False or None, the faster path: where two_kernel_path_supported, the top-k
+    with the page lookup and then the attention kernel
+    (dsa_topk_sparse_mla_fwd), else topk_select and sparse_mla_fwd.  The
+    results are the same every way.  Returns (out, lse, idx)."""
     b = buffers or {}
     num_q, H, _ = q.shape
     if num_splits is None:
@@ -383,6 +434,16 @@ def sparse_mla_topk(q, kv, kv_scale, block_table, q_req, q_pos, scores, k: int, 
                                      d_rope=d_rope, page_size=page_size, softmax_scale=softmax_scale,
                                      idx=b.get("idx"), out=b.get("out"), lse=b.get("lse"),
                                      workspace=b.get("workspace"), dev_status=dev_status, stream=stream)
+    if two_kernel_path_supported(H, d_latent, d_rope, scores.shape[1]):
+        r = topk_sparse_mla_fwd(q, kv, kv_scale, block_table, q_req, q_pos, scores, k, d_latent=d_latent,
+                                d_rope=d_rope, page_size=page_size, softmax_scale=softmax_scale,
+                                num_splits=num_splits, idx=b.get("idx"), out=b.get("out"), lse=b.get("lse"),
+                                o_part=b.get("o_part"), lse_part=b.get("lse_part"), workspace=b.get("workspace"),
+                                dev_status=dev_status, stream=stream)
+        if num_splits == 1:
+            return r
+        out, lse = combine(r[0], r[1], out=b.get("out"), lse=b.get("lse"), stream=stream)
+        return out, lse, r[2]
     idx = topk_select(scores, q_pos, k, idx=b.get("idx"), dev_status=dev_status, stream=stream,
                       workspace=b.get("topk_workspace"))
     if num_splits == 1:

@@ -206,6 +206,32 @@ dsa_status dsa_sparse_mla_topk_fwd(const float* scores, int64_t ld_scores, const
 
 int32_t dsa_sparse_mla_topk_max_k(void) { return dsa::mla_tc_fused_max_k(); }
 
+dsa_status dsa_topk_sparse_mla_fwd(const float* scores, int64_t ld_scores, const int32_t* q_pos, int32_t k,
+                                   int32_t* idx, const void* q, const uint8_t* kv, const float* kv_scale,
+                                   int64_t num_pages, const int32_t* block_table, int32_t num_req, int32_t bt_stride,
+                                   const int32_t* q_req, int32_t num_q, int32_t num_heads, int32_t d_latent,
+                                   int32_t d_rope, int32_t page_size, float softmax_scale, int32_t num_splits,
+                                   void* out, float* lse, float* o_part, float* lse_part, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (ld_scores <= 0 || k <= 0 || num_q < 0) return DSA_ERR_INVALID_ARG;
+  if (!use_tensor_cores(num_heads, d_latent, d_rope) || ld_scores > 65536) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (num_q == 0) return DSA_OK;
+  if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
+  dsa::MlaArgs a;
+  const size_t ws_need = dsa_sparse_mla_workspace_size(num_q, num_heads, d_latent, d_rope, k);
+  const dsa_status st = check_mla_args(q, kv, kv_scale, num_pages, block_table, num_req, bt_stride, q_req, idx,
+                                       num_q, num_heads, d_latent, d_rope, page_size, k, softmax_scale, num_splits,
+                                       out, lse, o_part, lse_part, ws_need, workspace, workspace_bytes, dev_status,
+                                       &a);
+  if (st != DSA_OK) return st;
+  const dsa::TopkResolve rv{static_cast<int2*>(workspace), block_table, q_req, kv_scale, num_pages, num_req,
+                            bt_stride, page_size};
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = dsa::launch_topk_resolve(scores, ld_scores, q_pos, num_q, k, idx, rv, dev_status, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(dsa::launch_mla_tc_resolved(a, workspace, s));
+}
+
 // Test hook, not part of include/dsa.h: the fp32 CUDA-core kernel on any
 // supported shape, so that tests can cross-check it against the tensor-core
 // kernel on the 64-head shape.  Same arguments as dsa_sparse_mla_fwd minus

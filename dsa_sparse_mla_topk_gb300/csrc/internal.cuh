@@ -18,6 +18,23 @@ size_t topk_workspace_bytes(int32_t num_q, int64_t ld, int32_t k);
 // CTAs per top-k row (a thread-block cluster) for this launch.
 int topk_cluster_size(int32_t num_q, int64_t ld, int num_sms);
 
+// The page lookup of the attention call folded into the top-k's write: for
+// every selected position its cache slot and dequantisation scale, as the
+// attention kernel reads them (slot -1 and scale 0 for padding and for bad
+// entries, which are reported as the attention call reports them).
+struct TopkResolve {
+  int2* res;  // [num_q, k]: (slot, scale bits)
+  const int32_t* block_table;
+  const int32_t* q_req;
+  const float* kv_scale;
+  int64_t num_pages;
+  int32_t num_req, bt_stride, page_size;
+};
+// Top-k of rows of at most 65,536 positions (ld <= 65,536) that also writes
+// rv.res; idx is written as launch_topk writes it.
+cudaError_t launch_topk_resolve(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
+                                int32_t* idx, const TopkResolve& rv, int32_t* dev_status, cudaStream_t stream);
+
 // SM count of the current device (cached per device).
 int device_sm_count();
 
@@ -49,6 +66,10 @@ cudaError_t launch_mla_simt(const MlaArgs& a, cudaStream_t stream);
 bool mla_tc_supported(const MlaArgs& a);
 size_t mla_tc_workspace_bytes(int32_t num_q, int32_t k);
 cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream);
+// The attention kernel alone, over entries launch_topk_resolve has just
+// written into `workspace` on the same stream (a programmatic dependent of
+// that top-k launch).
+cudaError_t launch_mla_tc_resolved(const MlaArgs& a, void* workspace, cudaStream_t stream);
 // Fused decode path: top-k of each token's scores row, then attention over
 // it, one CTA per token (one KV split; rows of at most 65,536 positions; k at
 // most mla_tc_fused_max_k()); `workspace` as for launch_mla_tc.

@@ -970,7 +970,10 @@ size_t mla_tc_workspace_bytes(int32_t num_q, int32_t k) {
   return sizeof(int2) * (size_t)num_q * (size_t)k;
 }
 
-cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream) {
+namespace {
+// resolve: launch the resolve kernel first (else `workspace` already holds the
+// entries, written by the kernel just before on the stream)
+cudaError_t launch_mla_tc_impl(const MlaArgs& a, void* workspace, cudaStream_t stream, bool resolve) {
   if (a.num_q == 0) return cudaSuccess;
   alignas(64) CUtensorMap map_lat, map_rope;
   if (!make_kv_map(&map_lat, a, 128, CU_TENSOR_MAP_SWIZZLE_128B) || !make_kv_map(&map_rope, a, DR, CU_TENSOR_MAP_SWIZZLE_64B))
@@ -989,14 +992,17 @@ cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream
   rcfg.stream = stream;
   rcfg.attrs = attr;
   rcfg.numAttrs = 1;
-  cudaError_t e = wide ? cudaLaunchKernelEx(&rcfg, resolve_kernel<8>, a, res)
-                       : cudaLaunchKernelEx(&rcfg, resolve_kernel<1>, a, res);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (resolve) {
+    e = wide ? cudaLaunchKernelEx(&rcfg, resolve_kernel<8>, a, res) : cudaLaunchKernelEx(&rcfg, resolve_kernel<1>, a, res);
+    if (e != cudaSuccess) return e;
+  }
   e = cudaFuncSetAttribute(mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the attention CTAs may start while the
-  // resolve kernel runs; they wait for it (griddepcontrol.wait) before
-  // reading its entries
+  // kernel before them (the resolve kernel, or the top-k that wrote the
+  // entries) runs; they wait for it (griddepcontrol.wait) before reading the
+  // entries
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_q, a.num_splits);
   cfg.blockDim = dim3(NTHREADS);
@@ -1007,6 +1013,15 @@ cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream
   e = cudaLaunchKernelEx(&cfg, mla_tc_kernel<false>, a, map_lat, map_rope, res, TopkIn{});
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_mla_tc(const MlaArgs& a, void* workspace, cudaStream_t stream) {
+  return launch_mla_tc_impl(a, workspace, stream, true);
+}
+
+cudaError_t launch_mla_tc_resolved(const MlaArgs& a, void* workspace, cudaStream_t stream) {
+  return launch_mla_tc_impl(a, workspace, stream, false);
 }
 
 int mla_tc_fused_max_k() { return FUSED_MAX_K; }

@@ -232,14 +232,15 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT, 2)
   }
 }
 
-enum RowMode { ROW_PLAIN = 0, ROW_SLICE = 1, ROW_MERGE = 2 };
+// ROW_RESOLVE: ROW_PLAIN that also writes each output's (slot, scale) pair.
+enum RowMode { ROW_PLAIN = 0, ROW_SLICE = 1, ROW_MERGE = 2, ROW_RESOLVE = 3 };
 constexpr uint32_t PAD_SCORE_BITS = 0xffc00000u;  // -NaN: its key is below every number's
 
 template <int MODE>
 __global__ void __launch_bounds__(RNT, 2)
     topk_row_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ q_pos, int32_t k,
                     int32_t* __restrict__ idx, int32_t* status, float* __restrict__ ws_score,
-                    int32_t* __restrict__ ws_pos, int nslices) {
+                    int32_t* __restrict__ ws_pos, int nslices, const TopkResolve rv) {
   extern __shared__ __align__(16) uint32_t rsm[];
   uint32_t* ckey = rsm;                                              // [RLCAP] candidate scores, then keys
   uint32_t* hist = ckey + RLCAP;                                     // [HBINS]
@@ -257,8 +258,49 @@ __global__ void __launch_bounds__(RNT, 2)
   const int tid = threadIdx.x;
   const int64_t row = MODE == ROW_SLICE ? blockIdx.x / nslices : blockIdx.x;
   const int64_t p = q_pos[row];
+  const int32_t r = MODE == ROW_RESOLVE ? rv.q_req[row] : 0;  // the row's request, for the lookups
   const bool bad = p < 0 || p >= ld;
   int32_t* out = idx + row * (int64_t)k;
+  // ROW_RESOLVE: outputs j of the row, at positions pos_of(j) (or -1), go to
+  // idx and, looked up in the block table, to rv.res; each of the two
+  // dependent loads (page, scale) is issued for four outputs at once
+  auto resolve_outputs = [&](auto pos_of) {
+    const bool req_ok = r >= 0 && r < rv.num_req;
+    int2* res = rv.res + row * (int64_t)k;
+    for (int j0 = tid; j0 < k; j0 += 4 * RNT) {
+      int32_t pos[4], page[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pos[e] = j0 + e * RNT < k ? pos_of(j0 + e * RNT) : -1;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        page[e] = -1;
+        if (pos[e] >= 0 && req_ok && pos[e] / rv.page_size < rv.bt_stride)
+          page[e] = rv.block_table[(int64_t)r * rv.bt_stride + pos[e] / rv.page_size];
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j0 + e * RNT;
+        int32_t slot = -1;
+        float sc = 0.f;
+        if (pos[e] >= 0) {
+          if (!req_ok) {
+            report(status, DSA_DEV_BAD_PAGE);
+          } else if (pos[e] / rv.page_size >= rv.bt_stride) {
+            report(status, DSA_DEV_BAD_INDEX);
+          } else if (page[e] < 0 || page[e] >= rv.num_pages) {
+            report(status, DSA_DEV_BAD_PAGE);
+          } else {
+            slot = page[e] * rv.page_size + pos[e] % rv.page_size;
+            sc = rv.kv_scale[slot];
+          }
+        }
+        if (j < k) {
+          out[j] = pos[e];
+          res[j] = make_int2(slot, __float_as_int(sc));
+        }
+      }
+    }
+  };
   const float* s;  // the scores this CTA selects from
   int vis;         // how many of them
   int64_t wbase = 0;
@@ -280,11 +322,26 @@ __global__ void __launch_bounds__(RNT, 2)
     if (MODE == ROW_MERGE) asm volatile("griddepcontrol.wait;" ::: "memory");  // the slices' blocks
     if (bad) {
       if (tid == 0) report(status, DSA_DEV_BAD_QPOS);
-      for (int j = tid; j < k; j += RNT) out[j] = -1;
+      if (MODE == ROW_RESOLVE)
+        resolve_outputs([](int) { return -1; });
+      else
+        for (int j = tid; j < k; j += RNT) out[j] = -1;
       return;
     }
+    if (MODE == ROW_RESOLVE && (tid >> 5) == RWARPS - 1 && r >= 0 && r < rv.num_req) {
+      // the request's block-table entries for the visible positions into L2
+      // for the lookups after the selection (one line per lane)
+      const int lane = tid & 31;
+      const int64_t nb = 4 * (int64_t)min((int64_t)rv.bt_stride, (p + rv.page_size) / rv.page_size);
+      const char* btrow = reinterpret_cast<const char*>(rv.block_table + (int64_t)r * rv.bt_stride);
+      for (int64_t off = lane * 128; off < nb; off += 32 * 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(btrow + off));
+      if (lane == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(btrow + nb - 1));  // an unaligned row's last line
+    }
     if (p + 1 <= k) {
-      for (int j = tid; j < k; j += RNT) out[j] = j < p + 1 ? j : -1;
+      if (MODE == ROW_RESOLVE)
+        resolve_outputs([&](int j) { return j < p + 1 ? j : -1; });
+      else
+        for (int j = tid; j < k; j += RNT) out[j] = j < p + 1 ? j : -1;
       return;
     }
     if (MODE == ROW_MERGE) {
@@ -303,7 +360,7 @@ __global__ void __launch_bounds__(RNT, 2)
   int32_t* chosen = reinterpret_cast<int32_t*>(ckey);
   const bool deferred = MODE != ROW_PLAIN && k <= RLCAP;
   auto emit = [&](uint32_t o, int32_t q) {
-    if (MODE == ROW_PLAIN) {
+    if (MODE == ROW_PLAIN || (MODE == ROW_RESOLVE && !deferred)) {
       out[o] = q;
     } else if (deferred) {
       chosen[o] = q;
@@ -315,7 +372,13 @@ __global__ void __launch_bounds__(RNT, 2)
     }
   };
   row_select(s, vis, k, emit, ckey, hist, above_bm, equal_bm, cpos, warp_buf, sel, minmax, wcount);
-  if (deferred) {
+  if (MODE == ROW_RESOLVE) {
+    __syncthreads();
+    if (deferred)
+      resolve_outputs([&](int j) { return chosen[j]; });
+    else
+      resolve_outputs([&](int j) { return __ldcg(out + j); });  // this CTA's own stores, before the barrier
+  } else if (deferred) {
     __syncthreads();
     if (MODE == ROW_SLICE) {
       for (int j = tid; j < k; j += RNT) {
@@ -368,7 +431,7 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos, i
         cudaFuncSetAttribute(topk_row_kernel<ROW_PLAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RSMEM);
     if (e != cudaSuccess) return e;
     topk_row_kernel<ROW_PLAIN><<<(unsigned)num_q, RNT, RSMEM, stream>>>(scores, ld, q_pos, k, idx, dev_status,
-                                                                        nullptr, nullptr, 1);
+                                                                        nullptr, nullptr, 1, TopkResolve{});
     return cudaGetLastError();
   }
   const size_t need = topk_workspace_bytes(num_q, ld, k);
@@ -385,7 +448,7 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos, i
     if (e != cudaSuccess) return e;
     topk_row_kernel<ROW_SLICE><<<(unsigned)num_q * slices, RNT, RSMEM, stream>>>(scores, ld, q_pos, k, idx,
                                                                                  dev_status, ws_score, ws_pos,
-                                                                                 slices);
+                                                                                 slices, TopkResolve{});
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -399,7 +462,7 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos, i
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, topk_row_kernel<ROW_MERGE>, scores, ld, q_pos, k, idx, dev_status, ws_score,
-                           ws_pos, slices);
+                           ws_pos, slices, TopkResolve{});
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
@@ -410,6 +473,18 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos, i
     case 2: return launch_c<2>(scores, ld, q_pos, num_q, k, idx, dev_status, stream);
     default: return launch_c<1>(scores, ld, q_pos, num_q, k, idx, dev_status, stream);
   }
+}
+
+cudaError_t launch_topk_resolve(const float* scores, int64_t ld, const int32_t* q_pos, int32_t num_q, int32_t k,
+                                int32_t* idx, const TopkResolve& rv, int32_t* dev_status, cudaStream_t stream) {
+  if (num_q == 0) return cudaSuccess;
+  if (ld > RMAXV) return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(topk_row_kernel<ROW_RESOLVE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RSMEM);
+  if (e != cudaSuccess) return e;
+  topk_row_kernel<ROW_RESOLVE><<<(unsigned)num_q, RNT, RSMEM, stream>>>(scores, ld, q_pos, k, idx, dev_status,
+                                                                          nullptr, nullptr, 1, rv);
+  return cudaGetLastError();
 }
 
 }  // namespace dsa

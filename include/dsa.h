@@ -224,6 +224,35 @@ DSA_API dsa_status dsa_sparse_mla_topk_fwd(const float* scores, int64_t ld_score
 DSA_API int32_t dsa_sparse_mla_topk_max_k(void);
 
 /*
+ * dsa_topk_sparse_mla_fwd -- dsa_topk_select followed by dsa_sparse_mla_fwd,
+ * with the attention call's first step (each selected position's page and
+ * dequantisation scale, looked up in the block table) done by the top-k
+ * kernel as it writes its indices: two kernels instead of three, the
+ * attention kernel a programmatic dependent of the top-k.  [LMSYS] section 3:
+ * the indexer's selection feeds the Partial step.  Same results, bit for bit,
+ * as the two calls, including dev_status: a bad q_pos sets DSA_DEV_BAD_QPOS;
+ * a position past the block table row DSA_DEV_BAD_INDEX; a page id or q_req
+ * out of range DSA_DEV_BAD_PAGE; such entries are attended as padding.
+ *
+ * Arguments are those of the two calls: scores, ld_scores, q_pos, k and idx
+ * as for dsa_topk_select (ld_scores at most 65,536), the rest as for
+ * dsa_sparse_mla_fwd (num_splits = 1 writes out / lse; num_splits > 1 writes
+ * o_part / lse_part for dsa_combine).  The workspace is
+ * dsa_sparse_mla_workspace_size() bytes (it receives the looked-up entries).
+ * Only the tensor-core shape (64, 512, 64) with ld_scores <= 65,536 is
+ * accepted; anything else returns DSA_ERR_UNSUPPORTED_SHAPE (the two calls
+ * take every shape).
+ */
+DSA_API dsa_status dsa_topk_sparse_mla_fwd(const float* scores, int64_t ld_scores, const int32_t* q_pos, int32_t k,
+                                           int32_t* idx, const void* q, const uint8_t* kv, const float* kv_scale,
+                                           int64_t num_pages, const int32_t* block_table, int32_t num_req,
+                                           int32_t bt_stride, const int32_t* q_req, int32_t num_q, int32_t num_heads,
+                                           int32_t d_latent, int32_t d_rope, int32_t page_size, float softmax_scale,
+                                           int32_t num_splits, void* out, float* lse, float* o_part,
+                                           float* lse_part, void* workspace, size_t workspace_bytes,
+                                           int32_t* dev_status, void* stream);
+
+/*
  * dsa_combine -- the DSA "Combine" step: exact log-sum-exp merge of split-KV
  * partial results.  [LMSYS] section 3: KV splits add intermediate writes and
  * Combine work.

@@ -175,6 +175,28 @@ def test_fused_argument_checks(lib, over, expect):
     assert _fused(lib, **over) == expect
 
 
+def _two(lib, **over):
+    a = dict(scores=FAKE, ld=4096, qpos=FAKE, k=2048, idx=FAKE, q=FAKE, kv=FAKE, kv_scale=FAKE, num_pages=4, bt=FAKE,
+             num_req=1, bt_stride=4, q_req=FAKE, num_q=1, H=64, dl=512, dr=64, P=64, scale=0.04, S=1, out=FAKE,
+             lse=FAKE, op=None, lp=None, ws=FAKE, wsb=1 << 20, st=None, stream=None)
+    a.update(over)
+    return lib.dsa_topk_sparse_mla_fwd(a["scores"], a["ld"], a["qpos"], a["k"], a["idx"], a["q"], a["kv"],
+                                       a["kv_scale"], a["num_pages"], a["bt"], a["num_req"], a["bt_stride"],
+                                       a["q_req"], a["num_q"], a["H"], a["dl"], a["dr"], a["P"], a["scale"], a["S"],
+                                       a["out"], a["lse"], a["op"], a["lp"], a["ws"], a["wsb"], a["st"], a["stream"])
+
+
+@no_device_only
+@pytest.mark.parametrize("over,expect", [
+    (dict(H=16, dl=64, dr=16), 2), (dict(ld=65537), 2), (dict(ld=0), 1), (dict(k=0), 1),
+    (dict(scores=None), 1), (dict(qpos=None), 1), (dict(idx=None), 1), (dict(out=None), 1), (dict(q=MISALIGNED), 1),
+    (dict(bt=None), 1), (dict(q_req=None), 1), (dict(S=0), 1), (dict(S=65), 1), (dict(S=4, op=None, lp=FAKE), 1),
+    (dict(wsb=100), 3), (dict(ws=None), 1), (dict(scale=float("nan")), 1), (dict(num_q=0), 0),
+])
+def test_two_kernel_argument_checks(lib, over, expect):
+    assert _two(lib, **over) == expect
+
+
 def test_fused_max_k(lib):
     assert lib.dsa_sparse_mla_topk_max_k() >= 2048
 

@@ -627,3 +627,78 @@ def test_topk_many_rows_persistent_path_bit_exact():
     assert (g[5] == -1).all()
     keep = np.arange(n) != 5
     assert np.array_equal(g[keep], ref[keep])
+
+
+def _separate_calls(inp, w, S, st, bt=None, q_req=None, q_pos=None):
+    kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+    idx = dsa.topk_select(inp.scores, inp.q_pos if q_pos is None else q_pos, w.k, dev_status=st)
+    r = dsa.sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table if bt is None else bt,
+                           inp.q_req if q_req is None else q_req, idx, num_splits=S, dev_status=st, **kw)
+    return r[0], r[1], idx
+
+
+def _two_kernels(inp, w, S, st, bt=None, q_req=None, q_pos=None):
+    kw = dict(d_latent=w.d_latent, d_rope=w.d_rope, page_size=w.page_size, softmax_scale=w.scale)
+    return dsa.topk_sparse_mla_fwd(inp.q, inp.kv, inp.kv_scale, inp.block_table if bt is None else bt,
+                                   inp.q_req if q_req is None else q_req, inp.q_pos if q_pos is None else q_pos,
+                                   inp.scores, w.k, num_splits=S, dev_status=st, **kw)
+
+
+@pytest.mark.parametrize("w,S", [(SMALL_H64, 1), (SMALL_H64, 3), (wl.DECODE_64K, 1), (wl.DECODE_64K, 2),
+                                 (wl.VERIFY_64K, 1), (wl.PREFILL_32K, 1)],
+                         ids=lambda v: v.name if isinstance(v, wl.Workload) else f"S{v}")
+def test_two_kernel_path_equals_separate_calls(w, S):
+    """dsa_topk_sparse_mla_fwd (the top-k also looking up each selected
+    position's page and scale, then the attention kernel) gives the indices,
+    outputs and LSE of dsa_topk_select + dsa_sparse_mla_fwd bit for bit (for
+    S > 1: the partial outputs and LSEs); the whole index array is compared."""
+    inp = inputs(w)
+    st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1, l1, i1 = _two_kernels(inp, w, S, st1)
+    o2, l2, i2 = _separate_calls(inp, w, S, st2)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == 0 and int(st2.item()) == 0
+    assert torch.equal(i1, i2)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_two_kernel_path_bad_inputs_match_separate_calls():
+    """Bad inputs on the two-kernel path: the same status bits and the same
+    outputs, bit for bit, as the separate calls (a q_pos out of range, a page
+    id out of range, a request id out of range, a block table too short for
+    the context)."""
+    w = SMALL_H64
+    inp = inputs(w)
+    last = w.num_q - 1
+    qp = inp.q_pos.clone()
+    qp[1] = inp.scores.shape[1] + 3
+    bt = inp.block_table.clone()
+    bt[0, 1] = 10 ** 6
+    q_req = inp.q_req.clone()
+    q_req[last] = w.num_req + 3
+    short_bt = inp.block_table[:, :20].contiguous()  # positions past 20 pages: BAD_INDEX
+    cases = [(dict(q_pos=qp), dsa.DEV_BAD_QPOS), (dict(bt=bt), dsa.DEV_BAD_PAGE),
+             (dict(q_req=q_req), dsa.DEV_BAD_PAGE), (dict(bt=short_bt), dsa.DEV_BAD_INDEX)]
+    for S in (1, 2):
+        for kw, flag in cases:
+            st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+            st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+            o1, l1, i1 = _two_kernels(inp, w, S, st1, **kw)
+            o2, l2, i2 = _separate_calls(inp, w, S, st2, **kw)
+            torch.cuda.synchronize()
+            assert int(st1.item()) == int(st2.item()) and int(st1.item()) & flag, (kw.keys(), S)
+            assert torch.equal(i1, i2) and torch.equal(o1, o2) and torch.equal(l1, l2), (kw.keys(), S)
+
+
+def test_two_kernel_path_rejects_other_shapes():
+    """The two-kernel entry point takes the tensor-core shape with rows of at
+    most 65,536 positions; sparse_mla_topk routes everything else to the
+    separate calls."""
+    w = SMALL_H16
+    inp = inputs(w)
+    assert not dsa.two_kernel_path_supported(w.heads, w.d_latent, w.d_rope, inp.scores.shape[1])
+    with pytest.raises(dsa.DsaError):
+        _two_kernels(inp, w, 1, None)
+    assert dsa.two_kernel_path_supported(64, 512, 64, 65536)
+    assert not dsa.two_kernel_path_supported(64, 512, 64, 65537)
