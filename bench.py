@@ -63,8 +63,8 @@ def parse_args():
     ap.add_argument("--max-blocks", type=int, default=400)
     ap.add_argument("--fused", action="store_true",
                     help="run top-k and attention in one kernel where the shape allows (slower than the default "
-                         "separate calls on every workload measured)")
-    ap.add_argument("--no-fused", action="store_true", help="separate calls (the default; kept for old commands)")
+                         "path on every workload measured)")
+    ap.add_argument("--no-fused", action="store_true", help="the default path (kept for old commands)")
     ap.add_argument("--splits", type=int, default=0, help="KV splits (0 = library's rule)")
     ap.add_argument("--cpu-sample", type=int, default=64, help="query tokens the oracle baseline times")
     ap.add_argument("--no-cpu-baseline", action="store_true")
