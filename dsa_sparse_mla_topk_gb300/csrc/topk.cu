@@ -277,11 +277,12 @@ __global__ void __launch_bounds__(RNT, 2)
         if (pos[e] >= 0 && req_ok && pos[e] / rv.page_size < rv.bt_stride)
           page[e] = rv.block_table[(int64_t)r * rv.bt_stride + pos[e] / rv.page_size];
       }
+      int32_t slot[4];
+      float sc[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int j = j0 + e * RNT;
-        int32_t slot = -1;
-        float sc = 0.f;
+        slot[e] = -1;
+        sc[e] = 0.f;
         if (pos[e] >= 0) {
           if (!req_ok) {
             report(status, DSA_DEV_BAD_PAGE);
@@ -290,13 +291,17 @@ __global__ void __launch_bounds__(RNT, 2)
           } else if (page[e] < 0 || page[e] >= rv.num_pages) {
             report(status, DSA_DEV_BAD_PAGE);
           } else {
-            slot = page[e] * rv.page_size + pos[e] % rv.page_size;
-            sc = rv.kv_scale[slot];
+            slot[e] = page[e] * rv.page_size + pos[e] % rv.page_size;
+            sc[e] = rv.kv_scale[slot[e]];
           }
         }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {  // the stores after all four scale loads
+        const int j = j0 + e * RNT;
         if (j < k) {
           out[j] = pos[e];
-          res[j] = make_int2(slot, __float_as_int(sc));
+          res[j] = make_int2(slot[e], __float_as_int(sc[e]));
         }
       }
     }
