@@ -122,7 +122,8 @@ constexpr int B_SYNCC = B_SYNCB + 1;
 constexpr int B_FIN = B_SYNCC + 1;        // every MMA is done (teardown)
 constexpr int B_QREADY = B_FIN + 1;       // Q hi/lo is in shared memory (and the Q staging stages are free)
 constexpr int B_QLOAD = B_QREADY + 1;     // raw bf16 Q has landed in the staging stages
-constexpr int NBAR = B_QLOAD + 1;
+constexpr int B_QEXP = B_QLOAD + 1;       // Q's power-of-two scale is in shared memory
+constexpr int NBAR = B_QEXP + 1;
 constexpr int QSTAGE = NST - 2;           // raw bf16 Q is staged in KV stages NST - 2 and NST - 1
 static_assert(2 * STAGE_BYTES == H * DQK * 2, "bf16 Q fills two KV stages");
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(bar(B_FIN), 1);
     mbar_init(bar(B_QREADY), NTHREADS / 32);
     mbar_init(bar(B_QLOAD), 1);
+    mbar_init(bar(B_QEXP), 1);
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -369,15 +371,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // KV stages) -> x 2^qexp -> E4M3 hi and lo.  The latent part goes to TMEM
   // (the QK^T A operand: row q_row(h, lo) in that lane, 4 bytes per column),
   // written by the warps of the row's lane quadrant; the rope part goes to
-  // shared memory (K-major, 64-byte swizzle).  All 16 warps take part (the
-  // TMA warps once the copies of tile 0 are out): qt numbers the threads;
-  // sync() is their barrier; with `arrive`, every warp arrives on B_QREADY
-  // at the end.
-  auto convert_q_by = [&](int qt, int nq, auto sync, bool arrive) {
-    constexpr int CH = DQK / 8;  // 16-byte chunks (8 bf16) per head
-    const uint4* qraw = reinterpret_cast<const uint4*>(smem + OFF_KV + QSTAGE * STAGE_BYTES);
-    auto bf_lo = [](uint32_t w) { return __uint_as_float(w << 16); };
-    auto bf_hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
+  // shared memory (K-major, 64-byte swizzle).  Two passes: the largest |Q|
+  // (q_max_pass: threads qt < nq, sync() their barrier; thread 0 writes the
+  // scale), then the split (q_split_pass, all 16 warps, the TMA warps once
+  // the copies of tile 0 are out; with `arrive`, every warp arrives on
+  // B_QREADY at the end).
+  constexpr int CH = DQK / 8;  // 16-byte chunks (8 bf16) per head
+  const uint4* qraw = reinterpret_cast<const uint4*>(smem + OFF_KV + QSTAGE * STAGE_BYTES);
+  auto bf_lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+  auto bf_hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
+  auto q_max_pass = [&](int qt, int nq, auto sync) {
     if (!wait_warp(B_QLOAD, 0)) ok = false;
     float mx = 0.f;
 #pragma unroll 4
@@ -398,7 +401,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (m > 0.f && m <= 3.0e38f) frexpf(m, &e);  // m < 2^e
       *qexp_s = (m > 0.f && m <= 3.0e38f) ? 8 - e : 0;
     }
-    sync();
+  };
+  auto q_split_pass = [&](int qt, int nq, bool arrive) {
     const float qs = ldexpf(1.f, *qexp_s);
     // hi and lo of 8 elements (one 16-byte chunk of raw Q), as byte quadruples
     auto split8 = [&](const uint4 v, uint2& hv, uint2& lv) {
@@ -458,7 +462,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncwarp();
     if (arrive && lane == 0) mbar_arrive(bar(B_QREADY));
   };
-  auto convert_q = [&](int qt) { convert_q_by(qt, NTHREADS, [] { named_barrier_sync(1, NTHREADS); }, true); };
+  auto convert_q_by = [&](int qt, int nq, auto sync, bool arrive) {
+    q_max_pass(qt, nq, sync);
+    sync();
+    q_split_pass(qt, nq, arrive);
+  };
+  // The plain kernel: the MMA and softmax warps (qt 224 .. 511) take the max
+  // pass alone as soon as Q has landed, so that the split can start before
+  // the TMA warps, busy with tile 0's copies, join it.
+  auto convert_q = [&](int qt) {
+    constexpr int NMX = NTHREADS - NTMA * 32;
+    if (qt >= NTMA * 32) {
+      q_max_pass(qt - NTMA * 32, NMX, [] { named_barrier_sync(4, NMX); });
+      if (qt == NTMA * 32) mbar_arrive(bar(B_QEXP));  // after writing the scale
+    } else if (!wait_warp(B_QLOAD, 0)) {
+      ok = false;
+    }
+    if (!wait_warp(B_QEXP, 0)) ok = false;
+    q_split_pass(qt, NTHREADS, true);
+  };
 
   // TMA warps: a tile's 80 copies (16 row groups of 4 rows x 4 latent slices
   // + 1 rope slice) are numbered group-major, c = 5 g + slice, and dealt out in
