@@ -52,8 +52,10 @@
 //  * A small resolve kernel first turns every selected position into its
 //    (slot, scale) pair, fully in parallel, into caller-provided scratch;
 //    the attention kernel is its programmatic dependent and overlaps it.
-//    The single-kernel variant (FUSED) selects its token's top k, resolves
-//    it and converts Q in its own prologue instead.
+//    On the two-kernel pass the top-k kernel writes those pairs itself and
+//    the attention kernel follows it directly.  The single-kernel variant
+//    (FUSED) selects its token's top k, resolves it and converts Q in its
+//    own prologue instead.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
