@@ -39,13 +39,13 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # as null once those sources change).
 TRAFFIC_BY_SOURCE: dict[str, dict[str, int]] = {
     # mla_tc.cu + topk_row.cuh: the single-kernel path (--fused: top-k + attention)
-    "dd9fcaf43cb3d9101d52cb958672ee4fa9e87447": {"decode_64k_prefix99.9": 84_476_928},
+    "c0c2a65f4ba5dd952ea20017545cbb7dad701f1e": {"decode_64k_prefix99.9": 84_461_824},
     # mla_tc.cu: the attention kernel as its own call; verify_64k_8tok's figure is
     # the 19-request capture (152 query tokens, one wave) scaled by 128 / 19
     # requests: the requests share no rows, so the traffic grows in proportion
-    "2f2ef12eb30385ad7f6cebf5d4e448bfde93abd4": {"decode_64k_prefix99.9": 49_768_704,
-                                                 "verify_64k_8tok_19req": 191_855_872,
-                                                 "verify_64k_8tok": 191_855_872 * 128 // 19},
+    "062c3281273413a49a357d84e58fbd63b9c04be3": {"decode_64k_prefix99.9": 49_795_840,
+                                                 "verify_64k_8tok_19req": 191_791_872,
+                                                 "verify_64k_8tok": 191_791_872 * 128 // 19},
 }
 
 
