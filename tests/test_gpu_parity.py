@@ -663,6 +663,27 @@ def test_two_kernel_path_equals_separate_calls(w, S):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+# k past the top-k's shared-memory candidate list (8,192): the selection falls
+# back to the exact select over the row, its outputs go straight to idx, and
+# the page lookup reads them back from there
+LARGE_K = wl.Workload("large_k9000_ctx20k", 2, 2, 64, 512, 64, 20000, 0, 64, 9000, seed=24,
+                      ctx_per_req=(20000, 9005))
+
+
+@pytest.mark.parametrize("S", [1, 3])
+def test_two_kernel_path_large_k(S):
+    w = LARGE_K
+    inp = inputs(w)
+    st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1, l1, i1 = _two_kernels(inp, w, S, st1)
+    o2, l2, i2 = _separate_calls(inp, w, S, st2)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == 0 and int(st2.item()) == 0
+    assert torch.equal(i1, i2) and torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert np.array_equal(host(i1), oracle.topk(host(inp.scores), host(inp.q_pos), w.k))
+
+
 def test_two_kernel_path_bad_inputs_match_separate_calls():
     """Bad inputs on the two-kernel path: the same status bits and the same
     outputs, bit for bit, as the separate calls (a q_pos out of range, a page
