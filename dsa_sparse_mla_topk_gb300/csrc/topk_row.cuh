@@ -293,8 +293,8 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
   };
 
   // ---- 0. loads in this order: a 1/16 sample (the first 32 of every 512
-  // positions), then the whole row into L2 (eight 16-byte-aligned pieces
-  // inside it) ----
+  // positions) and the stream's first half-batch; the whole row into L2
+  // (eight 16-byte-aligned pieces inside it) follows in step 1 ----
   const bool sampled = vis > RALL;
   constexpr int SPT = 8;  // sampled positions per thread: two float4s
   const int blk = (tid / (RS_RUN / SPT)) * RS_BLOCK + (tid % (RS_RUN / SPT)) * SPT;
@@ -311,16 +311,6 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
   // the stream's first half-batch is in flight during the threshold step
   float4 va[HB], vb[HB];
   load(va, 0);
-  if (tid < 8) {
-    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(s) + 15u) & ~uintptr_t(15);
-    const uintptr_t a1 = reinterpret_cast<uintptr_t>(s + vis) & ~uintptr_t(15);
-    if (a1 > a0) {
-      const uintptr_t piece = ((a1 - a0) / 8 + 15u) & ~uintptr_t(15);
-      const uintptr_t b0 = a0 + piece * (uintptr_t)tid;
-      const uintptr_t b1 = b0 + piece < a1 ? b0 + piece : a1;
-      if (b1 > b0) l2_prefetch_bulk(b0, (uint32_t)(b1 - b0));
-    }
-  }
   for (int b = tid; b < HBINS; b += RNT) hist[b] = 0u;
   for (int b = tid; b < RWORDS; b += RNT) {  // the two bitmaps need not be adjacent
     above_bm[b] = 0u;
@@ -335,6 +325,20 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
 #pragma unroll
     for (int t = 0; t < SPT; ++t)
       if (blk + t < vis) atomicAdd(&hist[score_key(sv[t]) >> 20], 1u);
+  }
+  // the whole row into L2, once this thread's sample has landed: issued at
+  // kernel start, the 128 rows' prefetches held back the samples
+  if (tid < 8) {
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(s) + 15u) & ~uintptr_t(15);
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(s + vis) & ~uintptr_t(15);
+    if (a1 > a0) {
+      const uintptr_t piece = ((a1 - a0) / 8 + 15u) & ~uintptr_t(15);
+      const uintptr_t b0 = a0 + piece * (uintptr_t)tid;
+      const uintptr_t b1 = b0 + piece < a1 ? b0 + piece : a1;
+      if (b1 > b0) l2_prefetch_bulk(b0, (uint32_t)(b1 - b0));
+    }
+  }
+  if (sampled) {
     const uint32_t ns = (uint32_t)(vis / RS_BLOCK) * RS_RUN + (uint32_t)min(vis % RS_BLOCK, RS_RUN);
     const float expect = (float)k * (float)ns / (float)vis;
     uint32_t need = (uint32_t)(expect * 1.25f) + 16u;
