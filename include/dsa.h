@@ -8,6 +8,10 @@
  *   scores --dsa_topk_select--> idx --dsa_sparse_mla_fwd--> (out, lse)
  *                                              \--(splits)--> partials --dsa_combine--> (out, lse)
  *
+ * dsa_topk_sparse_mla_fwd runs the first two calls as two kernels (the top-k
+ * also does the attention call's page lookup); dsa_sparse_mla_topk_fwd runs
+ * them as one kernel.  Both give the two calls' results bit for bit.
+ *
  * Sources (page titles):
  *  [LMSYS]  "Accelerating GLM-5.3-Flash on H200: High-Throughput Disaggregated
  *           Serving": section 1 "Architecture and workloads" (an indexer picks
