@@ -43,3 +43,20 @@ def test_tiny_workload_scores_have_exact_ties():
         vis = int(inp.q_pos[i]) + 1
         row = inp.scores[i, :vis]
         assert vis - torch.unique(row).numel() >= int(0.05 * vis) // 2
+
+
+def test_profiling_case_is_the_verify_block_on_fewer_requests():
+    """bench.py resolves workload names through workloads.lookup: the five
+    measured workloads, then the smaller profiling cases of the same kernels."""
+    v, v19 = wl.lookup("verify_64k_8tok"), wl.lookup("verify_64k_8tok_19req")
+    assert v is wl.VERIFY_64K
+    assert (v19.num_req, v19.num_q) == (19, 152)
+    for f in ("q_per_req", "heads", "d_latent", "d_rope", "ctx", "shared_prefix", "page_size", "k", "seed"):
+        assert getattr(v19, f) == getattr(v, f), f
+    assert set(wl.WORKLOADS).isdisjoint(wl.PROFILE_CASES)
+    try:
+        wl.lookup("no_such_workload")
+    except KeyError:
+        pass
+    else:
+        raise AssertionError("an unknown name must raise")
