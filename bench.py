@@ -39,7 +39,7 @@ FALLBACK_GBS, FALLBACK_TFLOPS = 6800.0, 1900.0
 # as null once those sources change).
 TRAFFIC_BY_SOURCE: dict[str, dict[str, int]] = {
     # mla_tc.cu + topk_row.cuh: the single-kernel path (--fused: top-k + attention)
-    "b7902350d77613bc2242782e95e27b8b75e874d2": {"decode_64k_prefix99.9": 84_849_152},
+    "a3ed308717ea26f427364930d9f7ab09e9d1a7d4": {"decode_64k_prefix99.9": 84_485_888},
     # mla_tc.cu: the attention kernel as its own call; verify_64k_8tok's figure is
     # the 19-request capture (152 query tokens, one wave) scaled by 128 / 19
     # requests: the requests share no rows, so the traffic grows in proportion

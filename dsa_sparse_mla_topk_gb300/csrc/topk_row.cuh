@@ -293,8 +293,8 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
   };
 
   // ---- 0. loads in this order: a 1/16 sample (the first 32 of every 512
-  // positions) and the stream's first half-batch; the whole row into L2
-  // (eight 16-byte-aligned pieces inside it) follows in step 1 ----
+  // positions) and the stream's first half-batch; the rest of the row into
+  // L2 (16-byte-aligned pieces inside it) follows in step 1 ----
   const bool sampled = vis > RALL;
   constexpr int SPT = 8;  // sampled positions per thread: two float4s
   const int blk = (tid / (RS_RUN / SPT)) * RS_BLOCK + (tid % (RS_RUN / SPT)) * SPT;
@@ -326,13 +326,14 @@ __device__ __forceinline__ void row_select(const float* s, int vis, int k, Emit 
     for (int t = 0; t < SPT; ++t)
       if (blk + t < vis) atomicAdd(&hist[score_key(sv[t]) >> 20], 1u);
   }
-  // the whole row into L2, once this thread's sample has landed: issued at
-  // kernel start, the 128 rows' prefetches held back the samples
-  if (tid < 8) {
-    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(s) + 15u) & ~uintptr_t(15);
+  // the rest of the row (past the first half-batch) into L2 in 16 pieces,
+  // once this thread's sample has landed: issued at kernel start, the 128
+  // rows' prefetches held back the samples
+  if (tid < 16) {
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(s4 + min(nv4, RNT * HB)) + 15u) & ~uintptr_t(15);
     const uintptr_t a1 = reinterpret_cast<uintptr_t>(s + vis) & ~uintptr_t(15);
     if (a1 > a0) {
-      const uintptr_t piece = ((a1 - a0) / 8 + 15u) & ~uintptr_t(15);
+      const uintptr_t piece = ((a1 - a0) / 16 + 15u) & ~uintptr_t(15);
       const uintptr_t b0 = a0 + piece * (uintptr_t)tid;
       const uintptr_t b1 = b0 + piece < a1 ? b0 + piece : a1;
       if (b1 > b0) l2_prefetch_bulk(b0, (uint32_t)(b1 - b0));
